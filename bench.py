@@ -1,0 +1,472 @@
+#!/usr/bin/env python3
+"""Benchmark of the decode-time skinny linears on GB300.
+
+Workload (the headline): the bf16 skinny GEMM sweep, y = x . W^T with
+M in {1,2,4,8,16,32,64,128} over (N,K) in {(4096,4096), (12288,4096), (4096,12288),
+(32768,1024), (8192,4096)}; x ~ N(0,1), W ~ N(0,1/K), seeded per shape, bf16.
+One step = one call of every one of those 40 shapes.
+
+Metric: microseconds per call and achieved HBM GB/s on weight bytes (fraction of
+the measured HBM peak) per (N,K,M); `value` is the whole step's weight bytes
+divided by its device time (GB/s).  The other hot-path workloads (the bf16 GEMV
+2048x1024 at M=1, fused gate/up, fp8 head + argmax, MoE W1/W2) are measured in the
+same run and reported under "ops".
+
+Timing: each shape's calls are captured in a CUDA graph of R back-to-back calls
+that rotate over enough weight copies to exceed 3x the L2 size (so no call finds
+its weights in L2); the graph is replayed once per step between CUDA events on the
+capturing stream; per-call time = event time / R.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+SWEEP_NK = [(4096, 4096), (12288, 4096), (4096, 12288), (32768, 1024), (8192, 4096)]
+SWEEP_M = [1, 2, 4, 8, 16, 32, 64, 128]
+GATE_UP_M = [1, 2, 3, 4, 6, 8, 12, 16, 32, 64, 128]
+HEAD_M = [1, 2, 3, 4, 8]
+MOE_M = [1, 2, 4, 8, 16]
+MOE_E, MOE_I, MOE_K, MOE_TOPK = 128, 1536, 4096, 6
+HEAD_N, HEAD_K = 248320, 4096
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD = ("bf16 skinny GEMM sweep M{1..128} x (N,K){(4096,4096),(12288,4096),(4096,12288),"
+            "(32768,1024),(8192,4096)}")
+METRIC = "µs/call and achieved HBM GB/s (% of GB300 peak) per (N,K,M) decode shape"
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_copy_gbs"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def _graph_case(torch, calls, reps: int, stream):
+    """Capture `reps` calls (a list of closures, used round-robin) into one CUDA graph."""
+    for c in calls[:2]:
+        c()                       # warm: attribute setup, occupancy cache
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for i in range(reps):
+            calls[i % len(calls)]()
+    torch.cuda.synchronize()
+    return g
+
+
+def _copies_for(nbytes: int, l2: int) -> int:
+    return max(2, -(-3 * l2 // max(1, nbytes)))
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import gemv_dg_bf16_gb300 as dg
+    from synth import decode_inputs as S
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    dg.dg_init(local)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+    peak, peak_src = _peaks()
+    stream = torch.cuda.Stream(device=dev)
+    R = args.reps
+
+    cases = []        # (name, dict(meta), graph, weight_bytes_per_call)
+
+    def add(name, meta, calls, wbytes):
+        with torch.cuda.stream(stream):
+            g = _graph_case(torch, calls, R, stream)
+        cases.append((name, meta, g, wbytes))
+
+    # --- the headline sweep
+    sweep_cases = []
+    for (N, K) in SWEEP_NK:
+        W0 = S.linear_inputs(1, N, K, device=dev)[1]
+        wb = N * K * 2
+        Ws = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)]
+        for M in SWEEP_M:
+            x = S.linear_inputs(M, N, K, device=dev)[0]
+            y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K, device=dev)
+            calls = [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Ws]
+            add("gemv_bf16", {"M": M, "N": N, "K": K}, calls, wb)
+            sweep_cases.append(len(cases) - 1)
+        del Ws, W0
+    if not args.sweep_only:
+        # --- GEMV 2048x1024 at M=1
+        N, K = 2048, 1024
+        x, W0 = S.linear_inputs(1, N, K, device=dev)
+        wb = N * K * 2
+        Ws = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)]
+        y = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
+        ws = dg.workspace(dg.DG_OP_GEMV_BF16, 1, N, K, device=dev)
+        add("gemv_bf16_2048x1024", {"M": 1, "N": N, "K": K},
+            [(lambda W=W: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Ws], wb)
+        # --- gate/up
+        Nh, K = 12288, 4096
+        W0 = S.gate_up_inputs(1, Nh, K, device=dev)[1]
+        wb = 2 * Nh * K * 2
+        Ws = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)]
+        for M in GATE_UP_M:
+            x = S.gate_up_inputs(M, Nh, K, device=dev)[0]
+            out = torch.empty((M, Nh), dtype=torch.bfloat16, device=dev)
+            ws = dg.workspace(dg.DG_OP_GATE_UP_SILU, M, Nh, K, device=dev)
+            add("gate_up_silu", {"M": M, "N_half": Nh, "K": K},
+                [(lambda W=W, x=x, out=out, ws=ws: dg.dg_gate_up_silu(x, W, out, ws=ws, stream=stream)) for W in Ws], wb)
+        del Ws, W0
+        # --- fp8 head
+        x8, Wq, scale = S.head_inputs(8, HEAD_N, HEAD_K, device=dev)
+        for M in HEAD_M:
+            x = x8[:M].contiguous()
+            logits = torch.empty((M, HEAD_N), dtype=torch.bfloat16, device=dev)
+            am = torch.empty((M,), dtype=torch.int32, device=dev)
+            ws = dg.workspace(dg.DG_OP_HEAD_FP8_ARGMAX, M, HEAD_N, HEAD_K, device=dev)
+            add("head_fp8_argmax", {"M": M, "N": HEAD_N, "K": HEAD_K},
+                [lambda x=x, logits=logits, am=am, ws=ws: dg.dg_head_fp8_argmax(
+                    x, Wq, scale, logits, am, ws=ws, stream=stream)], HEAD_N * HEAD_K + 4)
+        # --- MoE
+        W1q, s1, W2q, s2 = S.moe_weights(MOE_E, MOE_I, MOE_K, MOE_K, device=dev)
+        for M in MOE_M:
+            routs = [S.moe_inputs(M, MOE_K, MOE_TOPK, MOE_E, rep=r, device=dev) for r in range(8)]
+            uniq = [len(set(r[1].cpu().flatten().tolist())) for r in routs]
+            a = torch.empty((M, MOE_TOPK, MOE_I), dtype=torch.bfloat16, device=dev)
+            yv = torch.empty((M, MOE_K), dtype=torch.bfloat16, device=dev)
+            ws1 = dg.workspace(dg.DG_OP_MOE_W1, M, MOE_I, MOE_K, MOE_TOPK, device=dev)
+            ws2 = dg.workspace(dg.DG_OP_MOE_W2, M, MOE_K, MOE_I, MOE_TOPK, device=dev)
+            u_mean = sum(uniq) / len(uniq)
+            b1 = u_mean * (2 * MOE_I * MOE_K + 2 * MOE_I * 4)
+            b2 = u_mean * (MOE_K * MOE_I + MOE_K * 4)
+            add("moe_w1_silu", {"M": M, "U_mean": u_mean},
+                [(lambda r=r: dg.dg_moe_w1_silu(r[0], r[1], W1q, s1, a, ws=ws1, stream=stream)) for r in routs], b1)
+            add("moe_w2", {"M": M, "U_mean": u_mean},
+                [(lambda r=r: dg.dg_moe_w2(a, r[1], r[2], W2q, s2, yv, ws=ws2, stream=stream)) for r in routs], b2)
+
+    n_cases = len(cases)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_cases)]
+    times = [[] for _ in range(n_cases)]
+
+    def one_step(record):
+        for i, (_, _, g, _) in enumerate(cases):
+            if record:
+                ev[i][0].record(stream)
+            g.replay()
+            if record:
+                ev[i][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            one_step(False)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = ClockSampler(local)
+    clocks.start()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    step_ms = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.steps):
+            one_step(True)
+            stream.synchronize()
+            for i in range(n_cases):
+                times[i].append(ev[i][0].elapsed_time(ev[i][1]) * 1e3 / R)   # µs per call
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+
+    def summarize(i):
+        name, meta, _, wb = cases[i]
+        us = statistics.median(times[i])
+        gbs = wb / (us * 1e-6) / 1e9
+        return dict(op=name, **meta, us=round(us, 3), gbs=round(gbs, 1), frac=round(gbs / peak, 4),
+                    weight_bytes=int(wb))
+
+    sweep = [summarize(i) for i in sweep_cases]
+    step_us = sum(s["us"] for s in sweep)
+    step_bytes = sum(s["weight_bytes"] for s in sweep)
+    value_rank = step_bytes / (step_us * 1e-6) / 1e9
+    if world > 1:
+        t = torch.tensor([step_us], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_us = float(t.item())
+    value = world * step_bytes / (step_us * 1e-6) / 1e9
+    small = [s for s in sweep if s["M"] <= 16]
+    ops = {}
+    for i in range(n_cases):
+        if i in sweep_cases:
+            continue
+        s = summarize(i)
+        ops.setdefault(s["op"], []).append(s)
+
+    # ---- e2e through the public API with host buffers (x in, y out, pinned)
+    e2e = _e2e(torch, dg, S, dev, stream, args, l2)
+
+    launches = args.steps * R * n_cases
+    res = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_us / 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/K) weights; no dataset)",
+        "config": {"workload": WORKLOAD, "calls_per_step": len(sweep),
+                   "l2_defeat": f"weights rotate over >= 3x L2 ({l2 // 2**20} MiB) of copies inside "
+                                f"CUDA graphs of {R} calls",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(value_rank, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(value_rank / peak, 4), "traffic": _traffic(dg),
+                     "peak_source": peak_src, "kernel": "cc_dense_kernel (bf16 linear)",
+                     "frac_m_le_16": round(sum(s["weight_bytes"] for s in small) /
+                                           (sum(s["us"] for s in small) * 1e-6) / 1e9 / peak, 4)},
+        "clocks": clk,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "shapes": sweep,
+        "ops": ops,
+        "timed_wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res))
+
+
+def _e2e(torch, dg, S, dev, stream, args, l2):
+    """Whole sweep step through the Python API: pinned x -> device, call, y -> pinned host."""
+    items = []
+    h2d = d2h = wbytes = 0
+    for (N, K) in SWEEP_NK:
+        W = S.linear_inputs(1, N, K, device=dev)[1]
+        for M in SWEEP_M:
+            xh = S.linear_inputs(M, N, K)[0].pin_memory()
+            xd = torch.empty_like(xh, device=dev)
+            yd = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+            yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+            ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K, device=dev)
+            items.append((xh, xd, W, yd, yh, ws))
+            h2d += xh.numel() * 2
+            d2h += yh.numel() * 2
+            wbytes += N * K * 2
+
+    def step():
+        with torch.cuda.stream(stream):
+            for xh, xd, W, yd, yh, ws in items:
+                xd.copy_(xh, non_blocking=True)
+                dg.dg_gemv_bf16(xd, W, yd, ws=ws, stream=stream)
+                yh.copy_(yd, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        step()
+    n = max(3, min(args.steps, 50))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        step()
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(wbytes / dt / 1e9, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3),
+            "note": "weights stay resident (model parameters); per step each shape's x is copied "
+                    "in from pinned host memory and y copied back; wall clock incl. host overhead"}
+
+
+def _traffic(dg):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this build."""
+    p = os.path.join(ROOT, "profiles", "traffic_gemv_bf16.txt")
+    try:
+        kv = {}
+        with open(p) as f:
+            for ln in f:
+                if ":" in ln and not ln.startswith("#"):
+                    k, v = ln.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("build_id") != dg.dg_build_id():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ----------------------------------------------------------------------------- CPU baseline
+
+def _oracle_sweep_sample(budget_s: float, rows_frac: int = 64):
+    """Time the fp64 oracle on every sweep shape with every `rows_frac`-th weight row."""
+    import numpy as np
+    import torch
+
+    from oracle import oracle as O
+    from synth import decode_inputs as S
+
+    O.lib()
+    total_b = 0.0
+    total_t = 0.0
+    for (N, K) in SWEEP_NK:
+        rows = np.arange(0, N, rows_frac, dtype=np.int64)
+        g = torch.Generator().manual_seed(N * 7 + K)
+        Wsub = (torch.randn((len(rows), K), generator=g) * K ** -0.5).to(torch.bfloat16)
+        Wb = Wsub.view(torch.int16).numpy().view(np.uint16)
+        for M in SWEEP_M:
+            xb = S.linear_inputs(M, 8, K, tag="cpu")[0].view(torch.int16).numpy().view(np.uint16)
+            t0 = time.perf_counter()
+            O.linear_bf16(xb, Wb)
+            total_t += time.perf_counter() - t0
+            total_b += len(rows) * K * 2
+            if total_t > budget_s:
+                return total_b, total_t, f"every {rows_frac}th weight row of the sweep shapes (stopped at budget)"
+    return total_b, total_t, f"every {rows_frac}th weight row of all 40 sweep shapes"
+
+
+def cpu_baseline(budget_s: float):
+    b, t, sample = _oracle_sweep_sample(budget_s)
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": sample + f"; {t:.1f} s of fp64 oracle work, GB/s of weight bytes covered"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    budget = max(0.5, args.cpu_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _oracle_sweep_sample(budget, rows_frac=512)
+    b_tot = t_tot = 0.0
+    sample = ""
+    for _ in range(args.steps):
+        b, t, sample = _oracle_sweep_sample(budget, rows_frac=512)
+        b_tot += b
+        t_tot += t
+    value = b_tot / t_tot / 1e9
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    res = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+           "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": round(t_tot / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                            "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(res))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--reps", type=int, default=16, help="calls per captured graph")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--sweep-only", action="store_true", help="only the headline sweep (no other ops)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,278 @@
+"""ctypes marshalling for libdecodegemm.so.
+
+Tensors are torch tensors on the current CUDA device; their data pointers, the
+current stream and plain integers are passed through unchanged.  bf16 tensors
+are torch.bfloat16, e4m3 tensors are torch.uint8 (or float8_e4m3fn) codes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIBPATH = os.path.join(_HERE, "libdecodegemm.so")
+
+DG_OP_GEMV_BF16, DG_OP_GATE_UP_SILU, DG_OP_HEAD_FP8_ARGMAX, DG_OP_MOE_W1, DG_OP_MOE_W2 = range(5)
+DG_VAR_DEFAULT, DG_VAR_CC_WARP, DG_VAR_CC_BULK, DG_VAR_TC = range(4)
+
+
+def _rows_buckets():
+    with open(os.path.join(_HERE, "csrc", "dg_rows.h")) as f:
+        m = re.search(r"#define DG_ROWS_BUCKETS\(X\)\s+(.*)", f.read())
+    return tuple(int(v) for v in re.findall(r"X\((\d+)\)", m.group(1)))
+
+
+ROWS_BUCKETS = _rows_buckets()
+
+
+class Choice(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int32), ("params", ctypes.c_int32 * 6),
+                ("from_table", ctypes.c_int32), ("table_us", ctypes.c_float)]
+
+    @classmethod
+    def make(cls, variant: int, *params: int) -> "Choice":
+        c = cls()
+        c.variant = variant
+        for i, p in enumerate(params):
+            c.params[i] = p
+        return c
+
+    def as_tuple(self):
+        return (self.variant, tuple(self.params))
+
+    def __repr__(self):
+        return f"Choice(variant={self.variant}, params={list(self.params)}, from_table={self.from_table})"
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("op", ctypes.c_int32), ("M", ctypes.c_int32), ("N", ctypes.c_int32),
+                ("K", ctypes.c_int32), ("topk", ctypes.c_int32)]
+
+
+class DGError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {dg_status_str(status)} (status {status})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _LIBPATH
+
+
+def lib():
+    """Load the in-tree library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIBPATH):
+        raise ImportError(f"libdecodegemm.so is not built at {_LIBPATH}; run __graft_entry__.build()")
+    L = ctypes.CDLL(_LIBPATH)
+    P, I, Z, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_int
+    L.dg_init.argtypes = [I]
+    L.dg_status_str.argtypes = [S]
+    L.dg_status_str.restype = ctypes.c_char_p
+    L.dg_workspace_bytes.argtypes = [I, I, I, I, I]
+    L.dg_workspace_bytes.restype = Z
+    L.dg_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), P]
+    L.dg_device_status_clear.argtypes = [P, P]
+    L.dg_gemv_bf16.argtypes = [P, P, P, I, I, I, P, Z, P, P]
+    L.dg_gate_up_silu.argtypes = [P, P, P, I, I, I, P, Z, P, P]
+    L.dg_head_fp8_argmax.argtypes = [P, P, P, P, P, I, I, I, P, Z, P, P]
+    L.dg_moe_w1_silu.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
+    L.dg_moe_w2.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
+    L.dg_select.argtypes = [I, I, I, I, ctypes.POINTER(Choice)]
+    L.dg_table_load.argtypes = [ctypes.c_char_p]
+    L.dg_table_clear.argtypes = []
+    L.dg_table_clear.restype = None
+    L.dg_table_entries.argtypes = []
+    L.dg_selection_space.argtypes = []
+    L.dg_build_id.argtypes = []
+    L.dg_build_id.restype = ctypes.c_char_p
+    L.dg_table_check.argtypes = [ctypes.c_char_p, ctypes.c_char_p, I, I, ctypes.POINTER(ctypes.c_int),
+                                 ctypes.c_char_p, Z]
+    L.dg_sweep.argtypes = [ctypes.POINTER(Shape), I, ctypes.c_char_p, I]
+    for name in ("dg_init", "dg_device_status", "dg_device_status_clear", "dg_gemv_bf16",
+                 "dg_gate_up_silu", "dg_head_fp8_argmax", "dg_moe_w1_silu", "dg_moe_w2", "dg_select",
+                 "dg_table_load", "dg_table_check", "dg_sweep"):
+        getattr(L, name).restype = S
+    _lib = L
+    return L
+
+
+def dg_status_str(status: int) -> str:
+    return lib().dg_status_str(int(status)).decode()
+
+
+def _ok(status: int, where: str):
+    if status != 0:
+        raise DGError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _choice(choice):
+    if choice is None:
+        return None
+    if isinstance(choice, Choice):
+        return ctypes.byref(choice)
+    return ctypes.byref(Choice.make(*choice))
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def dg_init(device: int = 0):
+    _ok(lib().dg_init(int(device)), "dg_init")
+
+
+def dg_workspace_bytes(op: int, M: int, N: int, K: int, topk: int = 0) -> int:
+    return int(lib().dg_workspace_bytes(op, M, N, K, topk))
+
+
+def workspace(op: int, M: int, N: int, K: int, topk: int = 0, device=None) -> torch.Tensor:
+    """A zero-filled device workspace large enough for (op, M, N, K, topk)."""
+    n = dg_workspace_bytes(op, M, N, K, topk)
+    return torch.zeros(n, dtype=torch.uint8, device=device or torch.device("cuda"))
+
+
+def dg_device_status(ws: torch.Tensor, stream=None) -> int:
+    out = ctypes.c_int32(0)
+    _ok(lib().dg_device_status(_ptr(ws), ctypes.byref(out), _stream(stream)), "dg_device_status")
+    return int(out.value)
+
+
+def dg_device_status_clear(ws: torch.Tensor, stream=None):
+    _ok(lib().dg_device_status_clear(_ptr(ws), _stream(stream)), "dg_device_status_clear")
+
+
+def dg_gemv_bf16(x, W, y=None, ws=None, choice=None, stream=None):
+    """y[M,N] = x[M,K] . W[N,K]^T (bf16 in/out, fp32 accumulation)."""
+    M, K = x.shape
+    N = W.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(DG_OP_GEMV_BF16, M, N, K, device=x.device)
+    _check_dev(x, W, y, ws)
+    _ok(lib().dg_gemv_bf16(_ptr(x), _ptr(W), _ptr(y), M, N, K, _ptr(ws), ws.numel(), _stream(stream),
+                           _choice(choice)), "dg_gemv_bf16")
+    return y
+
+
+def dg_gate_up_silu(x, W_gu, out=None, ws=None, choice=None, stream=None):
+    """out[M,N_half] = silu(x . W_gu[0::2]^T) * (x . W_gu[1::2]^T)."""
+    M, K = x.shape
+    Nh = W_gu.shape[0] // 2
+    if out is None:
+        out = torch.empty((M, Nh), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(DG_OP_GATE_UP_SILU, M, Nh, K, device=x.device)
+    _check_dev(x, W_gu, out, ws)
+    _ok(lib().dg_gate_up_silu(_ptr(x), _ptr(W_gu), _ptr(out), M, Nh, K, _ptr(ws), ws.numel(),
+                              _stream(stream), _choice(choice)), "dg_gate_up_silu")
+    return out
+
+
+def dg_head_fp8_argmax(x, Wq, scale, logits=None, argmax=None, ws=None, choice=None, stream=None,
+                       want_logits=True):
+    """(logits[M,N] bf16 or None, argmax[M] int32) for the fp8 head with one scale."""
+    M, K = x.shape
+    N = Wq.shape[0]
+    if logits is None and want_logits:
+        logits = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if argmax is None:
+        argmax = torch.empty((M,), dtype=torch.int32, device=x.device)
+    if ws is None:
+        ws = workspace(DG_OP_HEAD_FP8_ARGMAX, M, N, K, device=x.device)
+    _check_dev(x, Wq, scale, logits, argmax, ws)
+    _ok(lib().dg_head_fp8_argmax(_ptr(x), _ptr(Wq), _ptr(scale), _ptr(logits), _ptr(argmax), M, N, K,
+                                 _ptr(ws), ws.numel(), _stream(stream), _choice(choice)),
+        "dg_head_fp8_argmax")
+    return logits, argmax
+
+
+def dg_moe_w1_silu(x, topk_ids, W1, s1, a=None, ws=None, choice=None, stream=None):
+    """a[M,topk,I] = silu(g) * u per routed slot."""
+    M, K = x.shape
+    topk = topk_ids.shape[1]
+    E, twoI, _ = W1.shape
+    I = twoI // 2
+    if a is None:
+        a = torch.empty((M, topk, I), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(DG_OP_MOE_W1, M, I, K, topk, device=x.device)
+    _check_dev(x, topk_ids, W1, s1, a, ws)
+    _ok(lib().dg_moe_w1_silu(_ptr(x), _ptr(topk_ids), _ptr(W1), _ptr(s1), _ptr(a), M, topk, E, I, K,
+                             _ptr(ws), ws.numel(), _stream(stream), _choice(choice)), "dg_moe_w1_silu")
+    return a
+
+
+def dg_moe_w2(a, topk_ids, topk_w, W2, s2, y=None, ws=None, choice=None, stream=None):
+    """y[M,Nout] = sum_k topk_w[t,k] * s2 * (a[t,k] . W2[e]^T)."""
+    M, topk, I = a.shape
+    E, Nout, _ = W2.shape
+    if y is None:
+        y = torch.empty((M, Nout), dtype=torch.bfloat16, device=a.device)
+    if ws is None:
+        ws = workspace(DG_OP_MOE_W2, M, Nout, I, topk, device=a.device)
+    _check_dev(a, topk_ids, topk_w, W2, s2, y, ws)
+    _ok(lib().dg_moe_w2(_ptr(a), _ptr(topk_ids), _ptr(topk_w), _ptr(W2), _ptr(s2), _ptr(y), M, topk, E,
+                        I, Nout, _ptr(ws), ws.numel(), _stream(stream), _choice(choice)), "dg_moe_w2")
+    return y
+
+
+def dg_select(op: int, M: int, N: int, K: int) -> Choice:
+    c = Choice()
+    _ok(lib().dg_select(op, M, N, K, ctypes.byref(c)), "dg_select")
+    return c
+
+
+def dg_table_load(path: str):
+    _ok(lib().dg_table_load(path.encode()), "dg_table_load")
+
+
+def dg_table_clear():
+    lib().dg_table_clear()
+
+
+def dg_table_entries() -> int:
+    return int(lib().dg_table_entries())
+
+
+def dg_selection_space() -> int:
+    return int(lib().dg_selection_space())
+
+
+def dg_build_id() -> str:
+    return lib().dg_build_id().decode()
+
+
+def dg_table_check(path: str, arch: str, driver_version: int, runtime_version: int):
+    """-> (status, entries, reason) without touching a GPU."""
+    n = ctypes.c_int(0)
+    buf = ctypes.create_string_buffer(512)
+    s = lib().dg_table_check(path.encode(), arch.encode(), driver_version, runtime_version,
+                             ctypes.byref(n), buf, 512)
+    return int(s), int(n.value), buf.value.decode()
+
+
+def dg_sweep(shapes, out_path: str, reps: int = 20):
+    """shapes: iterable of (op, M, N, K, topk)."""
+    arr = (Shape * len(shapes))(*[Shape(*s) for s in shapes])
+    _ok(lib().dg_sweep(arr, len(shapes), out_path.encode(), reps), "dg_sweep")

@@ -1,0 +1,461 @@
+// dg_api.cu -- the libdecodegemm C ABI: argument checks, kernel choice, launch.
+//
+// Nothing here allocates device memory or synchronises the host with a stream
+// (dg_device_status excepted, which exists for tests and health checks).
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "dg_cc_dense.cuh"
+#include "dg_internal.h"
+#include "dg_moe.cuh"
+
+namespace dg {
+
+namespace {
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+bool g_dev_ok[64];
+std::map<std::tuple<const void*, int, size_t>, int> g_occ;
+std::map<const void*, bool> g_attr;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+const DeviceInfo* current_device(dg_status* err)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        if (err) *err = DG_ERR_NO_DEVICE;
+        return nullptr;
+    }
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_dev_ok[dev]) return &g_dev[dev];
+    }
+    dg_status s = dg_init(dev);
+    if (s != DG_OK) {
+        if (err) *err = s;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    return &g_dev[dev];
+}
+
+int occupancy(const void* fn, int threads, size_t smem)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_attr[fn]) {
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxDynSmem));
+        g_attr[fn] = true;
+    }
+    auto key = std::make_tuple(fn, threads, smem);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    g_occ[key] = n;
+    return n;
+}
+
+void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
+{
+    (void)N;
+    (void)K;
+    std::memset(out, 0, sizeof *out);
+    out->variant = DG_VAR_CC_WARP;
+    switch (op) {
+    case DG_OP_GEMV_BF16:
+    case DG_OP_GATE_UP_SILU:
+        out->params[0] = M <= 2 ? 4 : (M <= 4 ? 4 : 2);
+        out->params[1] = 8;
+        break;
+    case DG_OP_HEAD_FP8_ARGMAX:
+        out->params[0] = M <= 2 ? 8 : (M <= 4 ? 4 : 4);
+        out->params[1] = 8;
+        break;
+    case DG_OP_MOE_W1:
+    case DG_OP_MOE_W2:
+        out->params[0] = 4;
+        out->params[1] = 8;
+        out->params[3] = 0;
+        break;
+    default:
+        break;
+    }
+}
+
+#ifndef DG_BUILD_ID
+#define DG_BUILD_ID "dev"
+#endif
+
+const char* build_id() { return DG_BUILD_ID; }
+
+}  // namespace dg
+
+using namespace dg;
+
+extern "C" {
+
+dg_status dg_init(int device)
+{
+    if (device < 0 || device >= 64) return DG_ERR_INVALID_ARG;
+    if (cudaSetDevice(device) != cudaSuccess) {
+        cudaGetLastError();
+        return DG_ERR_NO_DEVICE;
+    }
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) {
+        cudaGetLastError();
+        return DG_ERR_NO_DEVICE;
+    }
+    if (prop.major != 10 || prop.minor != 3) {
+        std::fprintf(stderr, "libdecodegemm: device %d is sm_%d%d; this build runs on sm_103 only\n",
+                     device, prop.major, prop.minor);
+        return DG_ERR_NO_DEVICE;
+    }
+    DeviceInfo info;
+    info.device = device;
+    info.sm_count = prop.multiProcessorCount;
+    info.cc_major = prop.major;
+    info.cc_minor = prop.minor;
+    info.max_smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+    cudaDriverGetVersion(&info.driver_version);
+    cudaRuntimeGetVersion(&info.runtime_version);
+    std::snprintf(info.name, sizeof info.name, "%s", prop.name);
+    bool first = false;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        first = !g_dev_ok[device];
+        g_dev[device] = info;
+        g_dev_ok[device] = true;
+    }
+    if (first) {
+        const char* path = std::getenv("DG_TABLE");
+        if (path && *path) dg_table_load(path);   // refusal prints one line; defaults stay
+    }
+    return DG_OK;
+}
+
+const char* dg_status_str(dg_status s)
+{
+    switch (s) {
+    case DG_OK: return "ok";
+    case DG_ERR_INVALID_ARG: return "invalid argument";
+    case DG_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case DG_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case DG_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case DG_ERR_CUDA: return "CUDA error";
+    case DG_ERR_TABLE_REFUSED: return "shape table refused";
+    case DG_ERR_NO_DEVICE: return "no usable sm_103 device";
+    case DG_ERR_BAD_VARIANT: return "bad kernel variant";
+    default: return "unknown status";
+    }
+}
+
+// Upper bound on the grid of any persistent dense launch (CTA partials of the head).
+static constexpr int kMaxGrid = 4096;
+
+size_t dg_workspace_bytes(dg_op op, int M, int N, int K, int topk)
+{
+    (void)K;
+    size_t b = kWsData;
+    switch (op) {
+    case DG_OP_HEAD_FP8_ARGMAX:
+        b += static_cast<size_t>(kMaxGrid) * 8 * 8;
+        break;
+    case DG_OP_MOE_W2:
+        if (M > 0 && topk > 0 && N > 0)
+            b += moe_terms_bytes(M, topk, N) + moe_ticket_bytes(M, N, 1);
+        break;
+    default:
+        break;
+    }
+    return b;
+}
+
+dg_status dg_device_status(const void* ws, int32_t* host_out, dg_stream_t stream)
+{
+    if (!ws || !host_out) return DG_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(host_out, static_cast<const uint8_t*>(ws) + kWsStatus, sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    return DG_OK;
+}
+
+dg_status dg_device_status_clear(void* ws, dg_stream_t stream)
+{
+    if (!ws) return DG_ERR_INVALID_ARG;
+    if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + kWsStatus, 0, sizeof(int32_t),
+                        reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    return DG_OK;
+}
+
+}  // extern "C"
+
+namespace dg {
+namespace {
+
+dg_status resolve_choice(dg_op op, int M, int N, int K, const dg_choice* in, dg_choice* out)
+{
+    if (in && in->variant != DG_VAR_DEFAULT) {
+        *out = *in;
+        return DG_OK;
+    }
+    return dg_select(op, M, N, K, out);
+}
+
+// Launch the dense CUDA-core family over token chunks.
+dg_status launch_dense(dg_op op, const DeviceInfo* dev, const dg_choice& c, DenseArgs a, int M,
+                       size_t ws_bytes, cudaStream_t stream)
+{
+    const int esz = (op == DG_OP_HEAD_FP8_ARGMAX) ? 1 : 2;
+    (void)esz;
+    int R = c.params[0] > 0 ? c.params[0] : 4;
+    const int wpc = c.params[1] > 0 ? c.params[1] : 8;
+    const int cap = c.params[2];
+    if ((R != 1 && R != 2 && R != 4 && R != 8) || wpc < 1 || wpc > 8 || cap < 0)
+        return DG_ERR_BAD_VARIANT;
+    if (op == DG_OP_GATE_UP_SILU && R < 2) return DG_ERR_BAD_VARIANT;
+    int mt_max = static_cast<int>(kXsBudget / (static_cast<size_t>(a.K) * 2));
+    if (mt_max > 8) mt_max = 8;
+    if (mt_max < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+    if (op == DG_OP_HEAD_FP8_ARGMAX && M > mt_max) return DG_ERR_UNSUPPORTED_SHAPE;
+    for (int t0 = 0; t0 < M; t0 += mt_max) {
+        const int mt = (M - t0 < mt_max) ? M - t0 : mt_max;
+        int r = R;
+        while (r > 1 && r * cpow2(mt) > 32) r >>= 1;       // same arithmetic, fewer rows per warp
+        if (op == DG_OP_GATE_UP_SILU && r < 2) return DG_ERR_UNSUPPORTED_SHAPE;
+        const void* fn = op == DG_OP_GEMV_BF16      ? dense_kernel_gemv(mt, r)
+                         : op == DG_OP_GATE_UP_SILU ? dense_kernel_gateup(mt, r)
+                                                    : dense_kernel_head(mt, r);
+        if (!fn) return DG_ERR_BAD_VARIANT;
+        const int threads = wpc * 32;
+        const size_t smem = static_cast<size_t>(mt) * a.K * 2;
+        int occ = occupancy(fn, threads, smem);
+        if (occ < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+        if (cap > 0 && occ > cap) occ = cap;
+        DenseArgs la = a;
+        la.t0 = t0;
+        la.groups = (a.N + r - 1) / r;
+        long long need = (la.groups + wpc - 1) / wpc;
+        long long grid = static_cast<long long>(dev->sm_count) * occ;
+        if (grid > need) grid = need;
+        if (grid > kMaxGrid) grid = kMaxGrid;
+        if (op == DG_OP_HEAD_FP8_ARGMAX &&
+            ws_bytes < kWsData + static_cast<size_t>(grid) * cpow2(mt) * 8)
+            return DG_ERR_WORKSPACE_TOO_SMALL;
+        void* args[] = {&la};
+        if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads), args, smem, stream) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return DG_ERR_CUDA;
+        }
+    }
+    return DG_OK;
+}
+
+dg_status check_common(const void* const* ptrs, int n, void* ws, size_t ws_bytes, size_t ws_need)
+{
+    for (int i = 0; i < n; ++i)
+        if (!ptrs[i]) return DG_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+        if (!aligned16(ptrs[i])) return DG_ERR_ALIGNMENT;
+    if (!ws) return DG_ERR_INVALID_ARG;
+    if (!aligned16(ws)) return DG_ERR_ALIGNMENT;
+    if (ws_bytes < ws_need) return DG_ERR_WORKSPACE_TOO_SMALL;
+    return DG_OK;
+}
+
+}  // namespace
+}  // namespace dg
+
+extern "C" {
+
+dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int K, void* ws,
+                       size_t ws_bytes, dg_stream_t stream, const dg_choice* choice)
+{
+    if (M < 1 || M > 128 || N < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (K % 8 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {x, W, y};
+    dg_status s = check_common(ptrs, 3, ws, ws_bytes, dg_workspace_bytes(DG_OP_GEMV_BF16, M, N, K, 0));
+    if (s != DG_OK) return s;
+    const DeviceInfo* dev = current_device(&s);
+    if (!dev) return s;
+    dg_choice c;
+    if ((s = resolve_choice(DG_OP_GEMV_BF16, M, N, K, choice, &c)) != DG_OK) return s;
+    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    DenseArgs a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.x = static_cast<const uint16_t*>(x);
+    a.N = N;
+    a.K = K;
+    a.out = static_cast<uint16_t*>(y);
+    a.ld_out = N;
+    a.ws = static_cast<uint8_t*>(ws);
+    return launch_dense(DG_OP_GEMV_BF16, dev, c, a, M, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_gate_up_silu(const void* x, const void* W_gu, void* out, int M, int N_half, int K,
+                          void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice)
+{
+    if (M < 1 || M > 128 || N_half < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (K % 8 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {x, W_gu, out};
+    dg_status s =
+        check_common(ptrs, 3, ws, ws_bytes, dg_workspace_bytes(DG_OP_GATE_UP_SILU, M, N_half, K, 0));
+    if (s != DG_OK) return s;
+    const DeviceInfo* dev = current_device(&s);
+    if (!dev) return s;
+    dg_choice c;
+    if ((s = resolve_choice(DG_OP_GATE_UP_SILU, M, N_half, K, choice, &c)) != DG_OK) return s;
+    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    DenseArgs a{};
+    a.W = static_cast<const uint8_t*>(W_gu);
+    a.x = static_cast<const uint16_t*>(x);
+    a.N = 2 * N_half;
+    a.K = K;
+    a.out = static_cast<uint16_t*>(out);
+    a.ld_out = N_half;
+    a.ws = static_cast<uint8_t*>(ws);
+    return launch_dense(DG_OP_GATE_UP_SILU, dev, c, a, M, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, void* logits,
+                             int32_t* argmax, int M, int N, int K, void* ws, size_t ws_bytes,
+                             dg_stream_t stream, const dg_choice* choice)
+{
+    if (M < 1 || M > 8 || N < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (K % 16 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!scale || !argmax) return DG_ERR_INVALID_ARG;
+    if (logits && !aligned16(logits)) return DG_ERR_ALIGNMENT;
+    const void* ptrs[] = {x, Wq};
+    dg_status s =
+        check_common(ptrs, 2, ws, ws_bytes, dg_workspace_bytes(DG_OP_HEAD_FP8_ARGMAX, M, N, K, 0));
+    if (s != DG_OK) return s;
+    const DeviceInfo* dev = current_device(&s);
+    if (!dev) return s;
+    dg_choice c;
+    if ((s = resolve_choice(DG_OP_HEAD_FP8_ARGMAX, M, N, K, choice, &c)) != DG_OK) return s;
+    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    DenseArgs a{};
+    a.W = static_cast<const uint8_t*>(Wq);
+    a.x = static_cast<const uint16_t*>(x);
+    a.N = N;
+    a.K = K;
+    a.out = static_cast<uint16_t*>(logits);
+    a.ld_out = N;
+    a.scale = scale;
+    a.argmax = argmax;
+    a.ws = static_cast<uint8_t*>(ws);
+    return launch_dense(DG_OP_HEAD_FP8_ARGMAX, dev, c, a, M, ws_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+static dg_status launch_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, MoeArgs a,
+                            cudaStream_t stream)
+{
+    const int wpc = c.params[1] > 0 ? c.params[1] : 8;
+    if (c.params[0] != 0 && c.params[0] != 4) return DG_ERR_BAD_VARIANT;
+    if (wpc < 1 || wpc > 8 || c.params[2] < 0 || c.params[3] < 0) return DG_ERR_BAD_VARIANT;
+    int tile = c.params[3];
+    if (tile == 0) tile = w1 ? wpc * 2 : wpc * 4;
+    a.tile = tile;
+    const void* fn = w1 ? moe_w1_kernel() : moe_w2_kernel();
+    const int threads = wpc * 32;
+    const size_t smem = static_cast<size_t>(8) * a.K * 2;
+    if (smem > kMaxDynSmem) return DG_ERR_UNSUPPORTED_SHAPE;
+    int occ = occupancy(fn, threads, smem);
+    if (occ < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+    if (c.params[2] > 0 && occ > c.params[2]) occ = c.params[2];
+    const long long grid = static_cast<long long>(dev->sm_count) * occ;
+    void* args[] = {&a};
+    if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads), args, smem, stream) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    return DG_OK;
+}
+
+dg_status dg_moe_w1_silu(const void* x, const int32_t* topk_ids, const void* W1, const float* s1,
+                         void* a_out, int M, int topk, int E, int I, int K, void* ws, size_t ws_bytes,
+                         dg_stream_t stream, const dg_choice* choice)
+{
+    if (M < 1 || M > 16 || topk < 1 || topk > 8 || E < 1 || E > 1024 || I < 1 || K < 1)
+        return DG_ERR_INVALID_ARG;
+    if (K % 16 != 0 || I % 8 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {x, topk_ids, W1, s1, a_out};
+    dg_status s = check_common(ptrs, 5, ws, ws_bytes, dg_workspace_bytes(DG_OP_MOE_W1, M, I, K, topk));
+    if (s != DG_OK) return s;
+    const DeviceInfo* dev = current_device(&s);
+    if (!dev) return s;
+    dg_choice c;
+    if ((s = resolve_choice(DG_OP_MOE_W1, M, I, K, choice, &c)) != DG_OK) return s;
+    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    MoeArgs a{};
+    a.x = static_cast<const uint16_t*>(x);
+    a.ids = topk_ids;
+    a.W = static_cast<const uint8_t*>(W1);
+    a.s = s1;
+    a.out = static_cast<uint16_t*>(a_out);
+    a.ws = static_cast<uint8_t*>(ws);
+    a.M = M;
+    a.topk = topk;
+    a.E = E;
+    a.I = I;
+    a.K = K;
+    a.Nout = 0;
+    return launch_moe(true, dev, c, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_moe_w2(const void* a_in, const int32_t* topk_ids, const float* gw, const void* W2,
+                    const float* s2, void* y, int M, int topk, int E, int I, int Nout, void* ws,
+                    size_t ws_bytes, dg_stream_t stream, const dg_choice* choice)
+{
+    if (M < 1 || M > 16 || topk < 1 || topk > 8 || E < 1 || E > 1024 || I < 1 || Nout < 1)
+        return DG_ERR_INVALID_ARG;
+    if (I % 16 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {a_in, topk_ids, gw, W2, s2, y};
+    dg_status s =
+        check_common(ptrs, 6, ws, ws_bytes, dg_workspace_bytes(DG_OP_MOE_W2, M, Nout, I, topk));
+    if (s != DG_OK) return s;
+    const DeviceInfo* dev = current_device(&s);
+    if (!dev) return s;
+    dg_choice c;
+    if ((s = resolve_choice(DG_OP_MOE_W2, M, Nout, I, choice, &c)) != DG_OK) return s;
+    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    MoeArgs a{};
+    a.x = static_cast<const uint16_t*>(a_in);
+    a.ids = topk_ids;
+    a.gw = gw;
+    a.W = static_cast<const uint8_t*>(W2);
+    a.s = s2;
+    a.out = static_cast<uint16_t*>(y);
+    a.ws = static_cast<uint8_t*>(ws);
+    a.M = M;
+    a.topk = topk;
+    a.E = E;
+    a.I = I;
+    a.K = I;
+    a.Nout = Nout;
+    return launch_moe(false, dev, c, a, reinterpret_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,292 @@
+// dg_cc_moe.cu -- small-M routed-expert GEMMs (W1 + SiLU.mul, W2 + combine) on
+// CUDA cores, split along N.
+//
+// "Decode optimization round 3", "Retained change 1: N-split W1/W2 MoE kernels":
+// at one to a few tokens only ~6 experts are active, so one CTA per expert (a
+// full-N tile) leaves most of the GPU idle; the experts' rows are instead cut
+// into many narrow N-tiles.  Here a work unit is (active expert, N-tile) and
+// persistent CTAs walk the unit list.  Routing is recomputed by every CTA from
+// topk_ids in shared memory (no host sync, no extra launch):
+//   a slot (t, k) is valid when 0 <= id < E and no earlier slot of t names id;
+//   active experts are listed in ascending id order; each expert's (token, slot)
+//   pairs are listed by ascending token then slot.
+// Arithmetic per output follows the canonical order of dg_common.cuh (e4m3
+// weights, 16 per vector).  W2's per-slot terms go through the workspace and
+// the CTA that finishes the last slot of a (token, N-tile) folds them in slot
+// order, so the combine is deterministic and needs no waiting.
+#include "dg_cc_dense.cuh"
+#include "dg_internal.h"
+#include "dg_moe.cuh"
+
+namespace dg {
+
+namespace {
+
+constexpr int kMoeR = 4;             // rows per warp group
+constexpr int kMoeMaxPairs = 128;    // M * topk
+constexpr int kMoeMaxE = 1024;
+constexpr int kMoeMT = 8;            // pairs per token chunk
+
+struct Route {
+    int U;                           // active experts
+    int P;                           // valid pairs
+    int nvalid[16];                  // valid slots per token
+    int16_t experts[kMoeMaxPairs];   // active expert ids, ascending
+    int16_t offs[kMoeMaxPairs + 1];  // pairs of active expert u: [offs[u], offs[u+1])
+    int8_t ptok[kMoeMaxPairs];
+    int8_t pslot[kMoeMaxPairs];
+    int8_t valid[kMoeMaxPairs];
+    int cnt[kMoeMaxE];               // per expert: pair count, then pair offset
+};
+
+// Every CTA computes the same routing tables (deterministic, no atomics on order).
+__device__ void route_scan(Route& R, const int32_t* __restrict__ ids, int M, int topk, int E,
+                           uint8_t* ws)
+{
+    const int P_all = M * topk;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) R.cnt[e] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < P_all; i += blockDim.x) {
+        const int t = i / topk, k = i - t * topk;
+        const int e = ids[i];
+        bool ok = e >= 0 && e < E;
+        for (int j = 0; ok && j < k; ++j)
+            if (ids[t * topk + j] == e) ok = false;
+        R.valid[i] = ok ? 1 : 0;
+        if (ok) atomicAdd(&R.cnt[e], 1);
+        else if (blockIdx.x == 0) set_status(ws, DG_DEVERR_BAD_TOPK_ID);
+    }
+    __syncthreads();
+    // Warp 0: exclusive scans over experts of (count > 0) and count.
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int carry_u = 0, carry_p = 0;
+        for (int base = 0; base < E; base += 32) {
+            const int e = base + lane;
+            const int c = e < E ? R.cnt[e] : 0;
+            const int a = c > 0 ? 1 : 0;
+            int su = a, sp = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int nu = __shfl_up_sync(kFull, su, o);
+                const int np = __shfl_up_sync(kFull, sp, o);
+                if (lane >= o) {
+                    su += nu;
+                    sp += np;
+                }
+            }
+            const int ex_u = carry_u + su - a, ex_p = carry_p + sp - c;
+            if (e < E) {
+                if (a) {
+                    R.experts[ex_u] = static_cast<int16_t>(e);
+                    R.offs[ex_u] = static_cast<int16_t>(ex_p);
+                }
+                R.cnt[e] = ex_p;    // now the expert's first pair position
+            }
+            carry_u += __shfl_sync(kFull, su, 31);
+            carry_p += __shfl_sync(kFull, sp, 31);
+        }
+        if (lane == 0) {
+            R.U = carry_u;
+            R.P = carry_p;
+            R.offs[carry_u] = static_cast<int16_t>(carry_p);
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < P_all; i += blockDim.x) {
+        if (!R.valid[i]) continue;
+        const int e = ids[i];
+        int rank = 0;
+        for (int j = 0; j < i; ++j)
+            if (R.valid[j] && ids[j] == e) ++rank;
+        const int pos = R.cnt[e] + rank;
+        R.ptok[pos] = static_cast<int8_t>(i / topk);
+        R.pslot[pos] = static_cast<int8_t>(i % topk);
+    }
+    for (int t = threadIdx.x; t < M; t += blockDim.x) {
+        int n = 0;
+        for (int k = 0; k < topk; ++k) n += R.valid[t * topk + k];
+        R.nvalid[t] = n;
+    }
+    __syncthreads();
+}
+
+// Stage `c` activation rows (one per pair, `kv` 16-byte vectors each) into xs.
+__device__ __forceinline__ void stage_rows(uint4* xs, const uint16_t* __restrict__ src,
+                                           const Route& R, int p0, int c, int kv, bool w1, int topk,
+                                           int K)
+{
+    for (int i = threadIdx.x; i < c * kv; i += blockDim.x) {
+        const int q = i / kv, v = i - q * kv;
+        const int t = R.ptok[p0 + q], k = R.pslot[p0 + q];
+        const size_t row = w1 ? static_cast<size_t>(t) : static_cast<size_t>(t) * topk + k;
+        xs[i] = *reinterpret_cast<const uint4*>(src + row * K + v * 8);
+    }
+}
+
+// W1 unit body for a chunk of MT pairs: gate rows j and up rows I + j of expert e.
+template <int MT>
+__device__ void w1_chunk(const MoeArgs& a, const Route& R, int e, int j_lo, int j_hi, int p0,
+                         const uint4* xs)
+{
+    constexpr int RH = kMoeR / 2;         // gate rows per group (and up rows)
+    constexpr int MTP = cpow2(MT);
+    constexpr int Q = kMoeR * MTP;
+    constexpr int SH = 5 - clog2(Q);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpc = blockDim.x >> 5;
+    const int idx = lane >> SH, my_r = idx / MTP, my_t = idx % MTP;
+    const bool writer = (lane & ((1 << SH) - 1)) == 0 && my_t < MT && my_r < RH;
+    const int kv = a.K / 8;
+    const uint8_t* We = a.W + static_cast<size_t>(e) * 2 * a.I * a.K;
+    for (int j0 = j_lo + warp * RH; j0 < j_hi; j0 += wpc * RH) {
+        const uint8_t* wrow[kMoeR];
+        bool rok[kMoeR];
+#pragma unroll
+        for (int r = 0; r < kMoeR; ++r) {
+            const int j = j0 + (r % RH);
+            rok[r] = j < j_hi;
+            const int row = (r < RH ? 0 : a.I) + (rok[r] ? j : j_lo);
+            wrow[r] = We + static_cast<size_t>(row) * a.K;
+        }
+        const float total = row_group_total<WT_E4M3, MT, kMoeR>(wrow, rok, a.K, xs, kv, lane);
+        // up partner of gate output (r, t) is (r + RH, t)
+        const float up = __shfl_sync(kFull, total, (lane + ((RH * MTP) << SH)) & 31);
+        const int j = j0 + my_r;
+        if (writer && j < j_hi) {
+            const float g = total * a.s[static_cast<size_t>(e) * 2 * a.I + j];
+            const float u = up * a.s[static_cast<size_t>(e) * 2 * a.I + a.I + j];
+            const float silu = g / (1.0f + expf(-g));
+            const int t = R.ptok[p0 + my_t], k = R.pslot[p0 + my_t];
+            a.out[(static_cast<size_t>(t) * a.topk + k) * a.I + j] = f32_to_bf16_bits(silu * u);
+        }
+    }
+}
+
+// W2 unit body for a chunk of MT pairs: rows n of expert e, terms to workspace.
+template <int MT>
+__device__ void w2_chunk(const MoeArgs& a, const Route& R, int e, int n_lo, int n_hi, int p0,
+                         const uint4* xs, float* terms)
+{
+    constexpr int MTP = cpow2(MT);
+    constexpr int Q = kMoeR * MTP;
+    constexpr int SH = 5 - clog2(Q);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, wpc = blockDim.x >> 5;
+    const int idx = lane >> SH, my_r = idx / MTP, my_t = idx % MTP;
+    const bool writer = (lane & ((1 << SH) - 1)) == 0 && my_t < MT;
+    const int kv = a.K / 8;   // K here is I (the W2 reduction length)
+    const uint8_t* We = a.W + static_cast<size_t>(e) * a.Nout * a.K;
+    for (int n0 = n_lo + warp * kMoeR; n0 < n_hi; n0 += wpc * kMoeR) {
+        const uint8_t* wrow[kMoeR];
+        bool rok[kMoeR];
+#pragma unroll
+        for (int r = 0; r < kMoeR; ++r) {
+            rok[r] = n0 + r < n_hi;
+            wrow[r] = We + static_cast<size_t>(rok[r] ? n0 + r : n_lo) * a.K;
+        }
+        const float total = row_group_total<WT_E4M3, MT, kMoeR>(wrow, rok, a.K, xs, kv, lane);
+        const int n = n0 + my_r;
+        if (writer && n < n_hi) {
+            const int t = R.ptok[p0 + my_t], k = R.pslot[p0 + my_t];
+            const float h = total * a.s[static_cast<size_t>(e) * a.Nout + n];
+            const float term = h * a.gw[t * a.topk + k];
+            terms[(static_cast<size_t>(t) * a.topk + k) * a.Nout + n] = term;
+        }
+    }
+}
+
+template <bool W1>
+__device__ void run_chunk(int c, const MoeArgs& a, const Route& R, int e, int lo, int hi, int p0,
+                          const uint4* xs, float* terms)
+{
+#define DG_MOE_CASE(MT)                                                       \
+    case MT:                                                                  \
+        if constexpr (W1) w1_chunk<MT>(a, R, e, lo, hi, p0, xs);              \
+        else w2_chunk<MT>(a, R, e, lo, hi, p0, xs, terms);                    \
+        break;
+    switch (c) {
+        DG_MOE_CASE(1) DG_MOE_CASE(2) DG_MOE_CASE(3) DG_MOE_CASE(4)
+        DG_MOE_CASE(5) DG_MOE_CASE(6) DG_MOE_CASE(7) DG_MOE_CASE(8)
+    default: break;
+    }
+#undef DG_MOE_CASE
+}
+
+template <bool W1>
+__global__ void __launch_bounds__(256) moe_kernel(MoeArgs a)
+{
+    __shared__ Route R;
+    __shared__ int fold_flag;
+    extern __shared__ uint4 xs[];        // [kMoeMT][K/8]
+    route_scan(R, a.ids, a.M, a.topk, a.E, a.ws);
+
+    const int rows = W1 ? a.I : a.Nout;                 // N-tiles cut these rows (W1: columns j)
+    const int tiles = (rows + a.tile - 1) / a.tile;
+    const int units = R.U * tiles;
+    const int kv = a.K / 8;
+    float* terms = reinterpret_cast<float*>(a.ws + kWsData);
+    unsigned* tickets = reinterpret_cast<unsigned*>(a.ws + kWsData + moe_terms_bytes(a.M, a.topk, a.Nout));
+
+    if constexpr (W1) {
+        // Invalid slots get a = 0 (no unit covers them).
+        if (blockIdx.x == 0)
+            for (int i = 0; i < a.M * a.topk; ++i)
+                if (!R.valid[i])
+                    for (int j = threadIdx.x; j < a.I; j += blockDim.x) a.out[static_cast<size_t>(i) * a.I + j] = 0;
+    } else {
+        // Tokens without a valid slot get y = 0 (nothing else writes them).
+        if (blockIdx.x == 0)
+            for (int t = 0; t < a.M; ++t)
+                if (R.nvalid[t] == 0)
+                    for (int n = threadIdx.x; n < a.Nout; n += blockDim.x) a.out[static_cast<size_t>(t) * a.Nout + n] = 0;
+    }
+
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+        const int ue = u / tiles, tile = u - ue * tiles;
+        const int e = R.experts[ue];
+        const int lo = tile * a.tile, hi = min(rows, lo + a.tile);
+        const int pb = R.offs[ue], pe = R.offs[ue + 1];
+        for (int p0 = pb; p0 < pe; p0 += kMoeMT) {
+            const int c = min(kMoeMT, pe - p0);
+            __syncthreads();                               // xs reuse
+            stage_rows(xs, a.x, R, p0, c, kv, W1, a.topk, a.K);
+            __syncthreads();
+            run_chunk<W1>(c, a, R, e, lo, hi, p0, xs, terms);
+        }
+        if constexpr (!W1) {
+            // Publish this unit's terms, then take a ticket per token of the unit.
+            __threadfence();
+            __syncthreads();
+            for (int p = pb; p < pe; ++p) {
+                const int t = R.ptok[p];
+                if (threadIdx.x == 0) {
+                    const unsigned old = atomicAdd(&tickets[t * tiles + tile], 1u);
+                    fold_flag = (old + 1 == static_cast<unsigned>(R.nvalid[t]));
+                }
+                __syncthreads();
+                if (fold_flag) {
+                    __threadfence();
+                    for (int n = lo + threadIdx.x; n < hi; n += blockDim.x) {
+                        float y = 0.0f;
+                        bool first = true;
+                        for (int k = 0; k < a.topk; ++k) {
+                            if (!R.valid[t * a.topk + k]) continue;
+                            const float v = ld_cg_f32(terms + (static_cast<size_t>(t) * a.topk + k) * a.Nout + n);
+                            y = first ? v : y + v;
+                            first = false;
+                        }
+                        a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
+                    }
+                    if (threadIdx.x == 0) tickets[t * tiles + tile] = 0u;
+                }
+                __syncthreads();
+            }
+        }
+    }
+}
+
+}  // namespace
+
+const void* moe_w1_kernel() { return reinterpret_cast<const void*>(&moe_kernel<true>); }
+const void* moe_w2_kernel() { return reinterpret_cast<const void*>(&moe_kernel<false>); }
+
+}  // namespace dg

@@ -1,0 +1,7 @@
+// Instantiations of the dense CUDA-core family for the fp8 head + greedy argmax.
+#include "dg_cc_dense.cuh"
+#include "dg_dense_table.cuh"
+
+namespace dg {
+const void* dense_kernel_head(int mt, int R) { return dense_lookup<WT_E4M3, EPI_HEAD>(mt, R); }
+}  // namespace dg

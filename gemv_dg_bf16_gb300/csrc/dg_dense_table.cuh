@@ -1,0 +1,53 @@
+// dg_dense_table.cuh -- maps (tokens per chunk, rows per warp) to a kernel
+// instantiation of cc_dense_kernel; only combinations whose R x pow2(MT) fits
+// one warp reduction (and, for gate/up, even R) are built.
+#pragma once
+
+#include "dg_cc_dense.cuh"
+
+namespace dg {
+
+template <int WT, int EPI, int MT, int R>
+constexpr bool dense_valid()
+{
+    return R * cpow2(MT) <= 32 && (EPI != EPI_GATEUP || (R % 2) == 0);
+}
+
+template <int WT, int EPI, int MT, int R>
+const void* dense_one()
+{
+    if constexpr (dense_valid<WT, EPI, MT, R>())
+        return reinterpret_cast<const void*>(&cc_dense_kernel<WT, MT, R, EPI>);
+    else
+        return nullptr;
+}
+
+template <int WT, int EPI, int MT>
+const void* dense_by_r(int R)
+{
+    switch (R) {
+    case 1: return dense_one<WT, EPI, MT, 1>();
+    case 2: return dense_one<WT, EPI, MT, 2>();
+    case 4: return dense_one<WT, EPI, MT, 4>();
+    case 8: return dense_one<WT, EPI, MT, 8>();
+    default: return nullptr;
+    }
+}
+
+template <int WT, int EPI>
+const void* dense_lookup(int mt, int R)
+{
+    switch (mt) {
+    case 1: return dense_by_r<WT, EPI, 1>(R);
+    case 2: return dense_by_r<WT, EPI, 2>(R);
+    case 3: return dense_by_r<WT, EPI, 3>(R);
+    case 4: return dense_by_r<WT, EPI, 4>(R);
+    case 5: return dense_by_r<WT, EPI, 5>(R);
+    case 6: return dense_by_r<WT, EPI, 6>(R);
+    case 7: return dense_by_r<WT, EPI, 7>(R);
+    case 8: return dense_by_r<WT, EPI, 8>(R);
+    default: return nullptr;
+    }
+}
+
+}  // namespace dg

@@ -1,0 +1,49 @@
+// dg_internal.h -- host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "dg.h"
+
+namespace dg {
+
+// Kernel entry points of the dense CUDA-core family, by (op, tokens in the
+// launch's chunk, rows per warp).  nullptr when that combination is not built.
+const void* dense_kernel_gemv(int mt, int R);
+const void* dense_kernel_gateup(int mt, int R);
+const void* dense_kernel_head(int mt, int R);
+
+// MoE kernels (rows per warp fixed per family; tokens per chunk chosen on device).
+const void* moe_w1_kernel();
+const void* moe_w2_kernel();
+
+struct DeviceInfo {
+    int device = -1;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int max_smem_optin = 0;
+    int driver_version = 0, runtime_version = 0;
+    char name[256] = {0};
+};
+
+// Properties of the current device (initialising it on first use); nullptr on failure.
+const DeviceInfo* current_device(dg_status* err);
+
+// Resident CTAs per SM for `fn` with `threads` threads and `smem` dynamic bytes
+// (cached); also raises the kernel's dynamic shared memory limit once.
+int occupancy(const void* fn, int threads, size_t smem);
+
+// Maximum dynamic shared memory any launch of this library asks for.
+constexpr size_t kMaxDynSmem = 200 * 1024;
+// Budget for staged activations of the dense CUDA-core family.
+constexpr size_t kXsBudget = 96 * 1024;
+
+// Compiled default choice for (op, M, N, K).
+void default_choice(dg_op op, int M, int N, int K, dg_choice* out);
+
+// Build identity string for tables.
+const char* build_id();
+
+}  // namespace dg

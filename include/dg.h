@@ -1,0 +1,238 @@
+/*
+ * dg.h -- libdecodegemm: decode-time skinny linear layers on GB300 (sm_103a).
+ *
+ * One C ABI for the five operations a decode step runs against large weight
+ * matrices with few token rows (M = 1..128):
+ *
+ *   dg_gemv_bf16        y = x . W^T, bf16 weights, bf16 out
+ *   dg_gate_up_silu     out = silu(x . W_gate^T) * (x . W_up^T), one launch
+ *   dg_head_fp8_argmax  fp8-e4m3 vocabulary head with one per-tensor scale,
+ *                       greedy (temperature 0) argmax fused into the same launch
+ *   dg_moe_w1_silu      routed-expert W1 (gate+up) with SiLU.mul, N-split
+ *   dg_moe_w2           routed-expert W2 with the gate-weighted combine, N-split
+ *
+ * plus dg_select, which maps (op, M, N, K) to a kernel variant through a
+ * per-device shape table written by an on-device sweep (dg_sweep).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor pointers are DEVICE pointers, row-major, densely packed, owned
+ *   by the caller.  bf16 values travel as their 16-bit patterns, e4m3 values as
+ *   their 8-bit codes (OCP 8-bit float E4M3, "fn" variant: no infinities,
+ *   S.1111.111 is NaN, largest magnitude 448).
+ * - Every pointer must be 16-byte aligned and K must be a multiple of 8
+ *   (bf16 weights) or 16 (e4m3 weights); otherwise DG_ERR_ALIGNMENT /
+ *   DG_ERR_UNSUPPORTED_SHAPE is returned before anything is launched.
+ * - Calls are asynchronous on `stream` and make no host synchronisation.
+ *   Argument errors are returned synchronously and launch nothing.
+ * - `ws` is a caller-owned device workspace of at least
+ *   dg_workspace_bytes(op, ...) bytes.  It must be zero-filled once when it is
+ *   allocated (e.g. cudaMemsetAsync); every call leaves its counters at zero
+ *   again.  Calls that share one workspace must be ordered on one stream.
+ *   The first 16 bytes hold a sticky device status word (dg_device_status).
+ * - `choice` may be NULL (dg_select picks); otherwise the given variant runs.
+ * - Accumulation is fp32 in a fixed order that does not depend on the kernel
+ *   variant, the launch geometry or the run: every variant dg_select can pick
+ *   for one (op, M, N, K) gives bitwise identical outputs.
+ * - The library allocates no device memory.  It keeps host-side state only:
+ *   per-device properties and the loaded shape table.
+ */
+#ifndef DG_H
+#define DG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* dg_stream_t;
+
+typedef enum {
+    DG_OK = 0,
+    DG_ERR_INVALID_ARG = 1,         /* null pointer, negative or zero size, bad topk/E */
+    DG_ERR_ALIGNMENT = 2,           /* a pointer is not 16-byte aligned */
+    DG_ERR_UNSUPPORTED_SHAPE = 3,   /* K not a multiple of the vector width, M too large, ... */
+    DG_ERR_WORKSPACE_TOO_SMALL = 4,
+    DG_ERR_CUDA = 5,                /* a CUDA runtime call or a launch failed */
+    DG_ERR_TABLE_REFUSED = 6,       /* a shape table failed its identity or knob checks */
+    DG_ERR_NO_DEVICE = 7,           /* no usable sm_103 device is current */
+    DG_ERR_BAD_VARIANT = 8          /* a dg_choice names a variant or params this op lacks */
+} dg_status;
+
+typedef enum {
+    DG_OP_GEMV_BF16 = 0,
+    DG_OP_GATE_UP_SILU = 1,
+    DG_OP_HEAD_FP8_ARGMAX = 2,
+    DG_OP_MOE_W1 = 3,
+    DG_OP_MOE_W2 = 4,
+    DG_OP_COUNT = 5
+} dg_op;
+
+/* Kernel families.  One family serves one (op, M) bucket; variants inside a
+ * family differ only in launch geometry and staging, never in arithmetic. */
+typedef enum {
+    DG_VAR_DEFAULT = 0,      /* let the library choose (same as choice == NULL) */
+    DG_VAR_CC_WARP = 1,      /* CUDA cores, each warp streams R weight rows through registers */
+    DG_VAR_CC_BULK = 2,      /* CUDA cores, bulk-async (TMA) copies stage weight rows in shared memory */
+    DG_VAR_TC = 3            /* tcgen05 tensor cores, TMA tiles, TMEM accumulators */
+} dg_variant;
+
+/* params[] meaning by variant:
+ *   DG_VAR_CC_WARP: [0] rows per warp R (1, 2, 4, 8), [1] warps per CTA (2..16),
+ *                   [2] CTAs per SM cap (0 = occupancy limit)
+ *   DG_VAR_CC_BULK: [0] rows per stage, [1] pipeline stages, [2] consumer warps
+ *   DG_VAR_TC:      [0] pipeline stages, [1] K-splits (0 = derived from the shape)
+ * For the MoE ops, params[3] is the N-tile width in rows (0 = derived). */
+typedef struct {
+    int32_t variant;
+    int32_t params[6];
+    int32_t from_table;      /* 1 when the choice came from a loaded shape table */
+    float table_us;          /* the table's measured time for this choice, else 0 */
+} dg_choice;
+
+/* Device status word values (sticky, OR-ed bits). */
+#define DG_DEVERR_BAD_TOPK_ID 0x1   /* a topk id was out of range or repeated in its row */
+#define DG_DEVERR_WAIT_TIMEOUT 0x2  /* a bounded pipeline wait gave up */
+
+/* ---------------------------------------------------------------- setup */
+
+/* Prepare the library for `device` (makes it current): checks for compute
+ * capability 10.3 and caches its properties, then loads the table named by
+ * the DG_TABLE environment variable, if any.  A refused table prints one line
+ * to stderr and leaves the compiled defaults in effect (the call still returns
+ * DG_OK).  Entry points call this lazily for the current device. */
+dg_status dg_init(int device);
+
+/* Human-readable name of a status code (static storage). */
+const char* dg_status_str(dg_status s);
+
+/* Workspace bytes an entry point needs.  N, K, topk by op:
+ *   GEMV_BF16:       N rows of W, K
+ *   GATE_UP_SILU:    N = N_half (output columns), K
+ *   HEAD_FP8_ARGMAX: N = vocabulary rows, K
+ *   MOE_W1:          N = I (expert intermediate), K = hidden, topk
+ *   MOE_W2:          N = Nout (hidden), K = I, topk
+ * Always >= 16 (the device status word). */
+size_t dg_workspace_bytes(dg_op op, int M, int N, int K, int topk);
+
+/* Copy the workspace's device status word to *host_out (synchronises `stream`;
+ * meant for tests and health checks, not the decode loop). */
+dg_status dg_device_status(const void* ws, int32_t* host_out, dg_stream_t stream);
+
+/* Clear the device status word (asynchronous on `stream`). */
+dg_status dg_device_status_clear(void* ws, dg_stream_t stream);
+
+/* ---------------------------------------------------------------- compute */
+
+/* Decode linear, mstar PR #1104 (decode GEMM table), "Why" / "What changed":
+ *   y[m, n] = bf16_rn( sum_k x[m, k] * W[n, k] )   fp32 accumulation
+ * x [M, K] bf16, W [N, K] bf16, y [M, N] bf16.  1 <= M <= 128. */
+dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int K,
+                       void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice);
+
+/* Fused gate/up projection with SiLU.mul, mstar PR #1104, "What changed"
+ * (the fused gate/up entry):
+ *   g = sum_k x[m,k] * W_gu[2j, k],  u = sum_k x[m,k] * W_gu[2j+1, k]   (fp32)
+ *   out[m, j] = bf16_rn( silu(g) * u ),  silu(g) = g / (1 + exp(-g))     (fp32)
+ * W_gu [2*N_half, K] bf16 stores gate row j at row 2j and up row j at 2j+1.
+ * out [M, N_half] bf16.  1 <= M <= 128. */
+dg_status dg_gate_up_silu(const void* x, const void* W_gu, void* out, int M, int N_half, int K,
+                          void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice);
+
+/* fp8 vocabulary head with greedy pick, mstar PR #1102 (fused draft step and
+ * fp8 draft head), "What changed" (one scale for all of the head; the pick at
+ * temperature 0 in the graph):
+ *   acc[m, n]   = sum_k x[m, k] * e4m3(Wq[n, k])        fp32
+ *   logit[m, n] = acc[m, n] * scale                      fp32 (one multiply)
+ *   logits[m,n] = bf16_rn(logit)                          (skipped if logits == NULL)
+ *   argmax[m]   = lowest n with the largest fp32 logit; NaN is never picked
+ *                 (a row of only NaN gives -1)
+ * x [M, K] bf16, Wq [N, K] e4m3 codes, scale: device pointer to one fp32,
+ * logits [M, N] bf16 or NULL, argmax [M] int32.  1 <= M <= 8.
+ * The argmax buffer is sized by this call's M. */
+dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, void* logits,
+                             int32_t* argmax, int M, int N, int K, void* ws, size_t ws_bytes,
+                             dg_stream_t stream, const dg_choice* choice);
+
+/* Routed-expert W1 with SiLU.mul, "Decode optimization round 3", "Retained
+ * change 1: N-split W1/W2 MoE kernels" (experts split along N at small M).
+ * A slot (t, k) is valid when 0 <= topk_ids[t, k] < E and no earlier slot of
+ * token t names the same expert.  For each valid slot, e = topk_ids[t, k]:
+ *   g = s1[e, j]     * sum_i x[t, i] * e4m3(W1[e, j, i])        fp32
+ *   u = s1[e, I + j] * sum_i x[t, i] * e4m3(W1[e, I + j, i])    fp32
+ *   a[t, k, j] = bf16_rn( silu(g) * u )
+ * Invalid slots write a = 0 and set DG_DEVERR_BAD_TOPK_ID in the status word.
+ * x [M, K] bf16, topk_ids [M, topk] int32, W1 [E, 2I, K] e4m3 (gate rows
+ * 0..I-1, up rows I..2I-1), s1 [E, 2I] fp32, a [M, topk, I] bf16.
+ * 1 <= M <= 16, 1 <= topk <= 8. */
+dg_status dg_moe_w1_silu(const void* x, const int32_t* topk_ids, const void* W1, const float* s1,
+                         void* a, int M, int topk, int E, int I, int K, void* ws, size_t ws_bytes,
+                         dg_stream_t stream, const dg_choice* choice);
+
+/* Routed-expert W2 with the gate-weighted combine (same page and section):
+ *   h[t, k, n] = s2[e, n] * sum_i a[t, k, i] * e4m3(W2[e, n, i])  fp32, e = topk_ids[t, k]
+ *   y[t, n]    = bf16_rn( sum over valid k, ascending: h[t, k, n] * gw[t, k] )  fp32
+ * a [M, topk, I] bf16, topk_ids [M, topk] int32, gw [M, topk] fp32,
+ * W2 [E, Nout, I] e4m3, s2 [E, Nout] fp32, y [M, Nout] bf16.
+ * 1 <= M <= 16, 1 <= topk <= 8; I must be a multiple of 16. */
+dg_status dg_moe_w2(const void* a, const int32_t* topk_ids, const float* gw, const void* W2,
+                    const float* s2, void* y, int M, int topk, int E, int I, int Nout, void* ws,
+                    size_t ws_bytes, dg_stream_t stream, const dg_choice* choice);
+
+/* ---------------------------------------------------------------- selection */
+
+/* Kernel choice for (op, M, N, K): the loaded table's entry for M padded up to
+ * the next row bucket (1 2 3 4 6 8 12 16 24 32 48 64 96 128), else the compiled
+ * default for that bucket -- never a nearest-bucket guess.  mstar PR #1104
+ * "What changed" (one per-device table; no table keeps the defaults);
+ * "Decode optimization round 3", "Retained change 2" (padded-M lookup). */
+dg_status dg_select(dg_op op, int M, int N, int K, dg_choice* out);
+
+/* Load a shape table (JSON written by dg_sweep).  The table's identity (device
+ * architecture, driver and runtime versions, library build id, selection-space
+ * token) must match this build and device, and no dispatch knob (DG_FORCE_VARIANT)
+ * may be set; otherwise DG_ERR_TABLE_REFUSED, one line on stderr, defaults stay.
+ * Strata PR #1297, "The second commit: the seam rework", items 1 and 2. */
+dg_status dg_table_load(const char* path);
+
+/* Drop the loaded table (defaults again). */
+void dg_table_clear(void);
+
+/* Number of entries in the loaded table (0 when none). */
+int dg_table_entries(void);
+
+/* Content hash of this library build (sources and compiler); tables record it. */
+const char* dg_build_id(void);
+
+/* The selection-space token of this build: it changes whenever the set of
+ * variants or their arithmetic changes, which makes older tables stale. */
+int dg_selection_space(void);
+
+/* Parse and check a table file without a GPU, against an explicit identity
+ * (for host-side tests and offline tools).  Returns the entry count through
+ * *entries and DG_OK, or DG_ERR_TABLE_REFUSED with a reason in reason[0..cap). */
+dg_status dg_table_check(const char* path, const char* arch, int driver_version,
+                         int runtime_version, int* entries, char* reason, size_t reason_cap);
+
+/* On-device sweep: for every op and shape in the request list, time every
+ * candidate variant, byte-compare its output with the default variant's and
+ * write a table that keeps every candidate's time and parameters beside the
+ * pick; a candidate replaces the default only if it is bitwise equal and at
+ * least 2 % faster.  mstar PR #1104, "What changed" (the promotion rule);
+ * Strata PR #1297, "Summary" and "True-default baseline".
+ * `shapes` is an array of n_shapes records {op, M, N, K, topk}; the sweep
+ * allocates and frees its own scratch buffers (it is an offline tool, not a
+ * decode-loop call).  Writes the JSON table to out_path. */
+typedef struct {
+    int32_t op, M, N, K, topk;
+} dg_shape;
+dg_status dg_sweep(const dg_shape* shapes, int n_shapes, const char* out_path, int reps);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DG_H */

@@ -1,0 +1,163 @@
+"""GPU parity of the bf16 linear and the fused gate/up against the fp64 oracle."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+import gemv_dg_bf16_gb300 as dg
+from oracle import oracle as O
+from oracle import tolerance as T
+from synth import decode_inputs as S
+from tests._helpers import bits16, f64, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+SWEEP_NK = [(4096, 4096), (12288, 4096), (4096, 12288), (32768, 1024), (8192, 4096)]
+SWEEP_M = [1, 2, 4, 8, 16, 32, 64, 128]
+GATE_UP_M = [1, 2, 3, 4, 6, 8, 12, 16, 32, 64, 128]
+
+
+def _lin_check(x, W, y, rows=None):
+    xb = bits16(x)
+    Wb = bits16(W if rows is None else W[torch.as_tensor(rows, device=W.device)])
+    ref, ad = O.linear_bf16(xb, Wb)
+    got = f64(y if rows is None else y[:, torch.as_tensor(rows, device=y.device)])
+    exc = T.linear_excess(got, ref, ad)
+    assert (exc <= 0).all(), f"max excess {exc.max():.3e} at {np.unravel_index(exc.argmax(), exc.shape)}"
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 2048, 1024), (3, 130, 1040), (5, 77, 520), (8, 300, 2056),
+                                   (16, 96, 264), (37, 65, 136), (128, 64, 1024), (2, 1, 8)])
+def test_gemv_small_exhaustive(cuda_device, M, N, K):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    y = dg.dg_gemv_bf16(x, W)
+    torch.cuda.synchronize()
+    _lin_check(x, W, y)
+
+
+@pytest.mark.parametrize("N,K", SWEEP_NK)
+@pytest.mark.parametrize("M", SWEEP_M)
+def test_gemv_sweep_full_size_sampled(cuda_device, M, N, K):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    y = dg.dg_gemv_bf16(x, W)
+    torch.cuda.synchronize()
+    _lin_check(x, W, y, rows=sample_rows(N, 96, seed=N + K + M))
+
+
+def _variants(op, mt_max):
+    out = []
+    for R, wpc, cap in itertools.product((1, 2, 4, 8), (2, 4, 8), (0, 1)):
+        if op == dg.DG_OP_GATE_UP_SILU and R < 2:
+            continue
+        out.append(dg.Choice.make(dg.DG_VAR_CC_WARP, R, wpc, cap))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 3080), (3, 515, 1024), (8, 256, 4096), (13, 70, 2048)])
+def test_gemv_variants_bitwise_identical(cuda_device, M, N, K):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    ref = dg.dg_gemv_bf16(x, W)
+    for c in _variants(dg.DG_OP_GEMV_BF16, 8):
+        y = dg.dg_gemv_bf16(x, W, choice=c)
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), repr(c)
+    for _ in range(3):
+        assert torch.equal(dg.dg_gemv_bf16(x, W).view(torch.int16), ref.view(torch.int16))
+
+
+def test_gemv_identity_and_one_hot_exact(cuda_device):
+    K = 1040
+    eye = torch.eye(K, dtype=torch.bfloat16, device=cuda_device)
+    x, W = S.linear_inputs(5, 300, K, device=cuda_device)
+    assert torch.equal(dg.dg_gemv_bf16(x, eye).view(torch.int16), x.view(torch.int16))
+    for k in (0, 517, K - 1):
+        e = torch.zeros((1, K), dtype=torch.bfloat16, device=cuda_device)
+        e[0, k] = 1.0
+        y = dg.dg_gemv_bf16(e, W)
+        assert torch.equal(y[0].view(torch.int16), W[:, k].contiguous().view(torch.int16))
+
+
+def test_gemv_writes_nothing_outside_y(cuda_device):
+    M, N, K = 3, 77, 520
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    buf = torch.full((M * N + 64,), 12345, dtype=torch.int16, device=cuda_device)
+    y = buf[8:8 + M * N].view(torch.bfloat16).view(M, N)   # 16-byte aligned view
+    dg.dg_gemv_bf16(x, W, y=y)
+    torch.cuda.synchronize()
+    assert (buf[:8] == 12345).all() and (buf[8 + M * N:] == 12345).all()
+    _lin_check(x, W, y)
+
+
+# ---------------------------------------------------------------- gate/up
+
+def _gate_up_check(x, Wgu, out, cols=None):
+    Nh = Wgu.shape[0] // 2
+    if cols is None:
+        r = O.gate_up_silu(bits16(x), bits16(Wgu))
+        got = f64(out)
+    else:
+        c = torch.as_tensor(cols, device=Wgu.device)
+        rows = torch.stack((2 * c, 2 * c + 1), dim=1).reshape(-1)
+        r = O.gate_up_silu(bits16(x), bits16(Wgu[rows]))
+        got = f64(out[:, c])
+    exc = T.silu_mul_excess(got, r["g"], r["u"], r["absg"], r["absu"], r["out"])
+    assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
+
+
+@pytest.mark.parametrize("M,Nh,K", [(1, 96, 1024), (3, 65, 1040), (6, 200, 520), (12, 33, 2048), (64, 16, 264)])
+def test_gate_up_small_exhaustive(cuda_device, M, Nh, K):
+    x, Wgu = S.gate_up_inputs(M, Nh, K, device=cuda_device)
+    out = dg.dg_gate_up_silu(x, Wgu)
+    torch.cuda.synchronize()
+    _gate_up_check(x, Wgu, out)
+
+
+@pytest.mark.parametrize("M", GATE_UP_M)
+def test_gate_up_full_size_sampled(cuda_device, M):
+    x, Wgu = S.gate_up_inputs(M, 12288, 4096, device=cuda_device)
+    out = dg.dg_gate_up_silu(x, Wgu)
+    torch.cuda.synchronize()
+    _gate_up_check(x, Wgu, out, cols=sample_rows(12288, 64, seed=M))
+
+
+def test_gate_up_variants_bitwise_identical(cuda_device):
+    x, Wgu = S.gate_up_inputs(6, 300, 2056, device=cuda_device)
+    ref = dg.dg_gate_up_silu(x, Wgu)
+    for c in _variants(dg.DG_OP_GATE_UP_SILU, 8):
+        out = dg.dg_gate_up_silu(x, Wgu, choice=c)
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), repr(c)
+
+
+def test_gate_up_matches_two_linears_plus_silu_on_device(cuda_device):
+    """out == bf16(silu(g)*u) with g, u the exact fp32 dot products: one-hot rows make g, u exact."""
+    K, Nh = 64, 8
+    Wf = torch.zeros((2 * Nh, K))
+    for j in range(Nh):
+        Wf[2 * j, j] = 1.0
+        Wf[2 * j + 1, 32 + j] = 1.0
+    x = torch.randn((2, K), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
+    out = dg.dg_gate_up_silu(x.to(cuda_device), Wf.to(torch.bfloat16).to(cuda_device))
+    g = x.float()[:, :Nh]
+    u = x.float()[:, 32:32 + Nh]
+    ref = (g / (1 + torch.exp(-g)) * u)
+    assert torch.allclose(out.float().cpu(), ref, rtol=2 ** -7, atol=1e-6)
+
+
+# ---------------------------------------------------------------- argument errors on device
+
+def test_bad_arguments_are_rejected_before_launch(cuda_device):
+    x, W = S.linear_inputs(2, 64, 256, device=cuda_device)
+    y = torch.empty((2, 64), dtype=torch.bfloat16, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GEMV_BF16, 2, 64, 256)
+    x2, W2 = S.linear_inputs(2, 64, 250, device=cuda_device)       # K not a multiple of 8
+    with pytest.raises(dg.DGError) as e:
+        dg.dg_gemv_bf16(x2, W2, y, ws=ws)
+    assert e.value.status == 3
+    raw = torch.empty(2 * 64 + 1, dtype=torch.bfloat16, device=cuda_device)
+    with pytest.raises(dg.DGError) as e:                           # output not 16-byte aligned
+        dg.dg_gemv_bf16(x, W, raw[1:].view(2, 64), ws=ws)
+    assert e.value.status == 2
+    with pytest.raises(dg.DGError) as e:                           # workspace too small
+        dg.dg_gemv_bf16(x, W, y, ws=ws[:8])
+    assert e.value.status == 4
+    torch.cuda.synchronize()

@@ -1,0 +1,120 @@
+"""GPU parity of the fp8-e4m3 vocabulary head and its fused greedy argmax."""
+import numpy as np
+import pytest
+import torch
+
+import gemv_dg_bf16_gb300 as dg
+from oracle import oracle as O
+from oracle import tolerance as T
+from synth import decode_inputs as S
+from tests._helpers import bits16, f64, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+HEAD_M = [1, 2, 3, 4, 8]
+
+
+def _check_logits(x, Wq, scale, logits, rows=None):
+    sc = float(scale.cpu()[0])
+    Wn = (Wq if rows is None else Wq[torch.as_tensor(rows, device=Wq.device)]).cpu().numpy()
+    lg, ad = O.head_fp8(bits16(x), Wn, sc)
+    got = f64(logits if rows is None else logits[:, torch.as_tensor(rows, device=logits.device)])
+    exc = T.linear_excess(got, lg, ad)
+    assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
+
+
+def _check_argmax(x, Wq, scale, am):
+    """Exact index unless the oracle's top-2 gap is within twice the error bound (then any
+    index whose exact logit is within that window of the maximum is accepted)."""
+    sc = float(scale.cpu()[0])
+    xb, Wn = bits16(x), Wq.cpu().numpy()
+    idx, best, gap = O.head_argmax(xb, Wn, sc)
+    got = am.cpu().numpy()
+    for m in range(x.shape[0]):
+        if got[m] == idx[m]:
+            continue
+        lg, ad = O.head_fp8(xb[m:m + 1], Wn, sc, rows=np.array([idx[m], got[m]]))
+        window = 2 * (T.REL * ad[0].max() + T.ABS)
+        assert gap[m] <= window and lg[0, 0] - lg[0, 1] <= window, (m, got[m], idx[m], gap[m])
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 4096), (2, 777, 1040), (3, 4099, 512), (5, 300, 2064),
+                                   (8, 2048, 4096), (4, 1, 16)])
+def test_head_small_exhaustive(cuda_device, M, N, K):
+    x, Wq, scale = S.head_inputs(M, N, K, device=cuda_device)
+    logits, am = dg.dg_head_fp8_argmax(x, Wq, scale)
+    torch.cuda.synchronize()
+    _check_logits(x, Wq, scale, logits)
+    _check_argmax(x, Wq, scale, am)
+
+
+@pytest.fixture(scope="module")
+def full_head(cuda_device):
+    x8, Wq, scale = S.head_inputs(8, 248320, 4096, device=cuda_device)
+    return x8, Wq, scale
+
+
+@pytest.mark.parametrize("M", HEAD_M)
+def test_head_full_size(cuda_device, full_head, M):
+    x8, Wq, scale = full_head
+    x = x8[:M].contiguous()
+    logits, am = dg.dg_head_fp8_argmax(x, Wq, scale)
+    torch.cuda.synchronize()
+    _check_logits(x, Wq, scale, logits, rows=sample_rows(248320, 128, seed=M))
+    _check_argmax(x, Wq, scale, am)
+    # the argmax-only call (no logits buffer) picks the same indices
+    _, am2 = dg.dg_head_fp8_argmax(x, Wq, scale, want_logits=False)
+    assert torch.equal(am, am2)
+
+
+def test_head_variants_bitwise_identical(cuda_device):
+    x, Wq, scale = S.head_inputs(5, 3001, 2064, device=cuda_device)
+    ref_l, ref_a = dg.dg_head_fp8_argmax(x, Wq, scale)
+    for R in (1, 2, 4, 8):
+        for wpc in (2, 4, 8):
+            for cap in (0, 1):
+                l, a = dg.dg_head_fp8_argmax(x, Wq, scale, choice=dg.Choice.make(dg.DG_VAR_CC_WARP, R, wpc, cap))
+                assert torch.equal(l.view(torch.int16), ref_l.view(torch.int16)), (R, wpc, cap)
+                assert torch.equal(a, ref_a)
+
+
+def test_head_ties_go_to_lowest_index(cuda_device):
+    M, N, K = 3, 5000, 1024
+    x, Wq, scale = S.head_inputs(M, N, K, device=cuda_device)
+    _, am = dg.dg_head_fp8_argmax(x, Wq, scale)
+    W2 = Wq.clone()
+    for m in range(M):
+        w = int(am[m])
+        W2[(w + 1234) % N] = Wq[w]            # a later (or wrapped earlier) copy of the winner
+    _, am2 = dg.dg_head_fp8_argmax(x, W2, scale)
+    for m in range(M):
+        w = int(am[m])
+        assert int(am2[m]) == min(w, (w + 1234) % N) or int(am2[m]) in (w, (w + 1234) % N) and \
+            int(am2[m]) == min(int(am2[m]), w, (w + 1234) % N)
+    zeros = torch.zeros_like(Wq)
+    l0, a0 = dg.dg_head_fp8_argmax(x, zeros, scale)
+    assert a0.tolist() == [0] * M and (l0.float() == 0).all()
+
+
+def test_head_nan_rows_never_win(cuda_device):
+    M, N, K = 2, 600, 512
+    x, Wq, scale = S.head_inputs(M, N, K, device=cuda_device)
+    _, am = dg.dg_head_fp8_argmax(x, Wq, scale)
+    W2 = Wq.clone()
+    for m in range(M):
+        W2[int(am[m]), 7] = 0x7F             # e4m3 NaN code
+    _, am2 = dg.dg_head_fp8_argmax(x, W2, scale)
+    idx, _, _ = O.head_argmax(bits16(x), W2.cpu().numpy(), float(scale.cpu()[0]))
+    assert am2.cpu().numpy().tolist() == idx.tolist()
+    allnan = torch.full_like(Wq, 0x7F)
+    _, a3 = dg.dg_head_fp8_argmax(x, allnan, scale)
+    assert a3.tolist() == [-1] * M
+
+
+def test_head_repeated_calls_reset_ticket(cuda_device):
+    x, Wq, scale = S.head_inputs(4, 10000, 1024, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_HEAD_FP8_ARGMAX, 4, 10000, 1024)
+    outs = [dg.dg_head_fp8_argmax(x, Wq, scale, ws=ws) for _ in range(5)]
+    for l, a in outs[1:]:
+        assert torch.equal(l.view(torch.int16), outs[0][0].view(torch.int16)) and torch.equal(a, outs[0][1])
+    assert dg.dg_device_status(ws) == 0

@@ -1,0 +1,140 @@
+"""GPU parity of the small-M MoE W1 (+SiLU.mul) and W2 (+combine), N-split."""
+import numpy as np
+import pytest
+import torch
+
+import gemv_dg_bf16_gb300 as dg
+from oracle import oracle as O
+from oracle import tolerance as T
+from synth import decode_inputs as S
+from tests._helpers import bits16, f64
+
+pytestmark = pytest.mark.gpu
+
+E, I, K, TOPK = 128, 1536, 4096, 6
+MOE_M = [1, 2, 4, 8, 16]
+
+
+@pytest.fixture(scope="module")
+def moe_w(cuda_device):
+    return S.moe_weights(E, I, K, K, device=cuda_device)
+
+
+def _compact(ids, *per_expert):
+    """Restrict weights to the experts the routing uses (ids renumbered, order kept)."""
+    ids_np = ids.cpu().numpy()
+    used = np.unique(ids_np[(ids_np >= 0) & (ids_np < E)])
+    remap = {int(e): i for i, e in enumerate(used)}
+    ids_c = np.vectorize(lambda e: remap.get(int(e), 10 ** 6))(ids_np).astype(np.int32)
+    sel = torch.as_tensor(used, device=per_expert[0].device)
+    return ids_c, [t[sel].cpu().numpy() for t in per_expert]
+
+
+def _w1_ref(x, ids, W1q, s1):
+    ids_c, (w1, sc1) = _compact(ids, W1q, s1)
+    return O.moe_w1_silu(bits16(x), ids_c, w1, sc1)
+
+
+def _w2_ref(a, ids, gw, W2q, s2):
+    ids_c, (w2, sc2) = _compact(ids, W2q, s2)
+    return O.moe_w2(bits16(a), ids_c, gw.cpu().numpy(), w2, sc2)
+
+
+@pytest.mark.parametrize("M", MOE_M)
+def test_moe_w1_full_size(cuda_device, moe_w, M):
+    W1q, s1, W2q, s2 = moe_w
+    x, ids, gw = S.moe_inputs(M, K, TOPK, E, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_MOE_W1, M, I, K, TOPK)
+    a = dg.dg_moe_w1_silu(x, ids, W1q, s1, ws=ws)
+    torch.cuda.synchronize()
+    r = _w1_ref(x, ids, W1q, s1)
+    exc = T.silu_mul_excess(f64(a), r["g"], r["u"], r["absg"], r["absu"], r["a"])
+    assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
+    assert dg.dg_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("M", MOE_M)
+def test_moe_w2_full_size_on_gpu_activations(cuda_device, moe_w, M):
+    W1q, s1, W2q, s2 = moe_w
+    x, ids, gw = S.moe_inputs(M, K, TOPK, E, device=cuda_device)
+    a = dg.dg_moe_w1_silu(x, ids, W1q, s1)
+    ws = dg.workspace(dg.DG_OP_MOE_W2, M, K, I, TOPK)
+    y = dg.dg_moe_w2(a, ids, gw, W2q, s2, ws=ws)
+    torch.cuda.synchronize()
+    ref, bound = _w2_ref(a, ids, gw, W2q, s2)
+    exc = T.linear_excess(f64(y), ref, bound)
+    assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
+    # repeated calls reuse the workspace tickets and give the same bits
+    for _ in range(3):
+        assert torch.equal(dg.dg_moe_w2(a, ids, gw, W2q, s2, ws=ws).view(torch.int16), y.view(torch.int16))
+    assert dg.dg_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_moe_tiles_and_warps_bitwise_identical(cuda_device, moe_w, M):
+    W1q, s1, W2q, s2 = moe_w
+    x, ids, gw = S.moe_inputs(M, K, TOPK, E, rep=7, device=cuda_device)
+    a_ref = dg.dg_moe_w1_silu(x, ids, W1q, s1)
+    y_ref = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2)
+    for wpc in (2, 4, 8):
+        for tile in (0, 8, 48, 1536):
+            c = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, wpc, 0, tile)
+            a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=c)
+            assert torch.equal(a.view(torch.int16), a_ref.view(torch.int16)), (wpc, tile)
+            c2 = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, wpc, 0, 4 * tile if tile else 0)
+            y = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2, choice=c2)
+            assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (wpc, tile)
+
+
+def test_moe_invalid_ids_flag_and_zero(cuda_device, moe_w):
+    W1q, s1, W2q, s2 = moe_w
+    M = 3
+    x, ids, gw = S.moe_inputs(M, K, TOPK, E, device=cuda_device)
+    bad = ids.clone()
+    bad[0, 2] = bad[0, 1]        # repeated expert
+    bad[1, 5] = 500              # out of range
+    bad[2, 0] = -3
+    ws = dg.workspace(dg.DG_OP_MOE_W1, M, I, K, TOPK)
+    a = dg.dg_moe_w1_silu(x, bad, W1q, s1, ws=ws)
+    assert dg.dg_device_status(ws) & 0x1
+    assert (a[0, 2] == 0).all() and (a[1, 5] == 0).all() and (a[2, 0] == 0).all()
+    dg.dg_device_status_clear(ws)
+    assert dg.dg_device_status(ws) == 0
+    ws2 = dg.workspace(dg.DG_OP_MOE_W2, M, K, I, TOPK)
+    y = dg.dg_moe_w2(a, bad, gw, W2q, s2, ws=ws2)
+    torch.cuda.synchronize()
+    assert dg.dg_device_status(ws2) & 0x1
+    # the oracle skips the same slots
+    ids_np = bad.cpu().numpy()
+    used = np.unique(ids_np[(ids_np >= 0) & (ids_np < E)])
+    remap = {int(e): i for i, e in enumerate(used)}
+    ids_c = np.array([[remap.get(int(e), -1) for e in row] for row in ids_np], np.int32)
+    sel = torch.as_tensor(used, device=cuda_device)
+    ref, bound = O.moe_w2(bits16(a), ids_c, gw.cpu().numpy(), W2q[sel].cpu().numpy(), s2[sel].cpu().numpy())
+    exc = T.linear_excess(f64(y), ref, bound)
+    assert (exc <= 0).all()
+
+
+def test_moe_token_without_valid_slot_gives_zero(cuda_device):
+    W1q, s1, W2q, s2 = S.moe_weights(8, 64, 256, 128, device=cuda_device)
+    x, ids, gw = S.moe_inputs(2, 256, 3, 8, device=cuda_device)
+    ids[1] = -1
+    a = dg.dg_moe_w1_silu(x, ids, W1q, s1)
+    y = dg.dg_moe_w2(a, ids, gw, W2q, s2)
+    torch.cuda.synchronize()
+    assert (y[1] == 0).all() and (a[1] == 0).all()
+    assert (y[0] != 0).any()
+
+
+def test_moe_single_expert_equals_scaled_gemv(cuda_device):
+    """One token, one slot, gate weight 1: W2 reduces to a per-row-scaled fp8 GEMV."""
+    W1q, s1, W2q, s2 = S.moe_weights(4, 512, 1024, 768, device=cuda_device)
+    a = torch.randn((1, 1, 512), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16).to(cuda_device)
+    ids = torch.tensor([[2]], dtype=torch.int32, device=cuda_device)
+    gw = torch.ones((1, 1), dtype=torch.float32, device=cuda_device)
+    y = dg.dg_moe_w2(a, ids, gw, W2q, s2)
+    torch.cuda.synchronize()
+    lg, ad = O.head_fp8(bits16(a[0]), W2q[2].cpu().numpy(), 1.0)
+    s = s2[2].cpu().numpy().astype(np.float64)
+    exc = T.linear_excess(f64(y), lg * s, ad * s)
+    assert (exc <= 0).all()

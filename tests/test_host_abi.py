@@ -1,0 +1,185 @@
+"""Host-side checks of the C ABI that need no GPU: exports, argument errors, the shape
+table parser and its refusals, bucket padding and the dispatch knob."""
+import ctypes
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import gemv_dg_bf16_gb300 as dg
+from gemv_dg_bf16_gb300 import _binding as B
+from tests._helpers import ROOT, header_functions
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from gemv_dg_bf16_gb300 import build
+    build.build()
+    return dg.lib()
+
+
+def test_library_exports_every_declared_function():
+    names = header_functions()
+    assert len(names) >= 18
+    L = ctypes.CDLL(dg.library_path())
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_library_has_no_oracle_dependency():
+    out = subprocess.run(["nm", "-D", dg.library_path()], capture_output=True, text=True).stdout
+    assert "dgo_" not in out
+
+
+def test_rows_buckets_one_list():
+    assert dg.ROWS_BUCKETS == (1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128)
+
+
+def test_status_strings():
+    assert dg.dg_status_str(0) == "ok"
+    assert "aligned" in dg.dg_status_str(2)
+    assert dg.dg_status_str(99) == "unknown status"
+
+
+# Fake device addresses: every call below fails an argument check before any launch.
+A = 0x10000            # 16-byte aligned
+U = 0x10002            # misaligned
+
+
+def _gemv(x=A, W=A, y=A, M=2, N=64, K=256, ws=A, wsb=4096):
+    return dg.lib().dg_gemv_bf16(ctypes.c_void_p(x), ctypes.c_void_p(W), ctypes.c_void_p(y), M, N, K,
+                                 ctypes.c_void_p(ws), wsb, None, None)
+
+
+def test_argument_errors_before_any_device_work():
+    assert _gemv(M=0) == 1
+    assert _gemv(M=129) == 1
+    assert _gemv(K=250) == 3
+    assert _gemv(x=0) == 1
+    assert _gemv(W=U) == 2
+    assert _gemv(ws=U) == 2
+    assert _gemv(wsb=8) == 4
+    L = dg.lib()
+    P = ctypes.c_void_p
+    assert L.dg_head_fp8_argmax(P(A), P(A), None, P(A), P(A), 2, 100, 64, P(A), 1 << 20, None, None) == 1
+    assert L.dg_head_fp8_argmax(P(A), P(A), P(A), P(A), P(A), 9, 100, 64, P(A), 1 << 20, None, None) == 1
+    assert L.dg_head_fp8_argmax(P(A), P(A), P(A), P(A), P(A), 2, 100, 40, P(A), 1 << 20, None, None) == 3
+    assert L.dg_head_fp8_argmax(P(A), P(A), P(A), P(U), P(A), 2, 100, 64, P(A), 1 << 20, None, None) == 2
+    assert L.dg_moe_w1_silu(P(A), P(A), P(A), P(A), P(A), 17, 6, 128, 1536, 4096, P(A), 1 << 20, None, None) == 1
+    assert L.dg_moe_w1_silu(P(A), P(A), P(A), P(A), P(A), 2, 9, 128, 1536, 4096, P(A), 1 << 20, None, None) == 1
+    assert L.dg_moe_w2(P(A), P(A), P(A), P(A), P(A), P(A), 2, 6, 128, 1544, 4096, P(A), 1 << 24, None, None) == 3
+    assert L.dg_moe_w2(P(A), P(A), P(A), P(A), P(A), P(A), 2, 6, 128, 1536, 4096, P(A), 64, None, None) == 4
+
+
+def test_workspace_sizes():
+    assert dg.dg_workspace_bytes(dg.DG_OP_GEMV_BF16, 1, 4096, 4096) >= 16
+    assert dg.dg_workspace_bytes(dg.DG_OP_HEAD_FP8_ARGMAX, 8, 248320, 4096) >= 256 + 4096 * 8 * 8
+    w2 = dg.dg_workspace_bytes(dg.DG_OP_MOE_W2, 16, 4096, 1536, 6)
+    assert w2 >= 16 * 6 * 4096 * 4
+
+
+def test_select_defaults_and_bucket_padding():
+    for op in range(5):
+        for M in (1, 5, 7, 100, 128):
+            c = dg.dg_select(op, M, 4096, 4096)
+            assert c.variant == dg.DG_VAR_CC_WARP and c.from_table == 0
+    with pytest.raises(dg.DGError):
+        dg.dg_select(0, 129, 4096, 4096)
+    # a bucket's default does not depend on where in the bucket M falls
+    assert dg.dg_select(0, 5, 64, 64).as_tuple() == dg.dg_select(0, 6, 64, 64).as_tuple()
+
+
+# ---------------------------------------------------------------- shape table
+
+ARCH, DRV, RT = "sm_103", 13000, 13000
+
+
+def _table(tmp_path, **over):
+    ident = {"arch": ARCH, "driver": DRV, "runtime": RT, "build": dg.dg_build_id(),
+             "selection_space": dg.dg_selection_space()}
+    ident.update(over.pop("identity", {}))
+    for k in over.pop("drop", []):
+        ident.pop(k)
+    entries = over.pop("entries", [
+        {"op": "gemv_bf16", "M": 1, "N": 4096, "K": 4096,
+         "pick": {"variant": 1, "params": [2, 4, 0, 0, 0, 0]}, "pick_us": 5.0,
+         "default": {"variant": 1, "params": [4, 8, 0, 0, 0, 0]}, "default_us": 5.2,
+         "candidates": [{"variant": 1, "params": [4, 8, 0, 0, 0, 0], "us": 5.2, "bitwise": True},
+                        {"variant": 1, "params": [2, 4, 0, 0, 0, 0], "us": 5.0, "bitwise": True}]},
+        {"op": "moe_w2", "M": 16, "N": 4096, "K": 1536,
+         "pick": {"variant": 1, "params": [4, 8, 0, 64, 0, 0]}, "pick_us": 50.0}])
+    doc = {"format": "libdecodegemm-table", "identity": ident, "entries": entries}
+    doc.update(over)
+    p = tmp_path / "table.json"
+    p.write_text(json.dumps(doc))
+    return str(p)
+
+
+def _check(path, **kw):
+    return dg.dg_table_check(path, kw.get("arch", ARCH), kw.get("drv", DRV), kw.get("rt", RT))
+
+
+def test_table_valid(tmp_path):
+    s, n, why = _check(_table(tmp_path))
+    assert (s, n) == (0, 2), why
+
+
+@pytest.mark.parametrize("kw,needle", [
+    (dict(drop=["selection_space"]), "made before the kernel selection space"),
+    (dict(identity={"selection_space": 99}), "selection space 99"),
+    (dict(identity={"arch": "sm_100"}), "architecture sm_100"),
+    (dict(identity={"driver": 12080}), "driver 12080"),
+    (dict(identity={"runtime": 1}), "runtime 1"),
+    (dict(identity={"build": "0123"}), "library build 0123"),
+    (dict(entries=[{"op": "gemv_bf16", "M": 5, "N": 1, "K": 8, "pick": {"variant": 1, "params": [4, 8]}}]),
+     "not a decode bucket"),
+    (dict(entries=[{"op": "gemv_bf16", "M": 4, "N": 1, "K": 8, "pick": {"variant": 7, "params": [4, 8]}}]),
+     "selection space"),
+    (dict(entries=[{"op": "gate_up_silu", "M": 4, "N": 1, "K": 8, "pick": {"variant": 1, "params": [1, 8]}}]),
+     "even"),
+    (dict(entries=[{"op": "nope", "M": 4, "N": 1, "K": 8, "pick": {"variant": 1, "params": [4, 8]}}]),
+     "unknown op"),
+    (dict(entries=[{"op": "gemv_bf16", "M": 4, "N": 1, "K": 8}]), "pick"),
+    (dict(format="other"), "not a libdecodegemm table"),
+])
+def test_table_refusals(tmp_path, kw, needle):
+    s, n, why = _check(_table(tmp_path, **kw))
+    assert s == 6 and n == 0 and needle in why, why
+
+
+def test_table_corrupt_and_truncated(tmp_path):
+    good = _table(tmp_path)
+    text = open(good).read()
+    bad = tmp_path / "trunc.json"
+    bad.write_text(text[: len(text) // 2])
+    s, _, why = _check(str(bad))
+    assert s == 6 and "not a valid table" in why
+    s, _, why = _check(str(tmp_path / "missing.json"))
+    assert s == 6 and "cannot read" in why
+    garbage = tmp_path / "garbage.json"
+    garbage.write_bytes(b"\x00\xff{{{")
+    assert _check(str(garbage))[0] == 6
+
+
+def test_table_refused_when_dispatch_knob_set(tmp_path):
+    path = _table(tmp_path)
+    code = ("import sys; sys.path.insert(0, %r); import gemv_dg_bf16_gb300 as dg; "
+            "s, n, why = dg.dg_table_check(%r, 'sm_103', 13000, 13000); print(s, why)") % (ROOT, path)
+    env = dict(os.environ, DG_FORCE_VARIANT="1:2,4,0,0")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True).stdout
+    assert out.startswith("6 ") and "DG_FORCE_VARIANT" in out
+
+
+def test_force_knob_drives_select():
+    code = ("import sys; sys.path.insert(0, %r); import gemv_dg_bf16_gb300 as dg; "
+            "c = dg.dg_select(0, 3, 64, 64); print(c.variant, list(c.params))") % ROOT
+    env = dict(os.environ, DG_FORCE_VARIANT="1:2,4,1,0")
+    out = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, check=True).stdout
+    assert out.split() [:3] == ["1", "[2,", "4,"]
+    env = dict(os.environ, DG_FORCE_VARIANT="5:1,1,0,0")
+    code_bad = code.replace("c = dg.dg_select(0, 3, 64, 64); print(c.variant, list(c.params))",
+                            "print(dg.lib().dg_select(0, 3, 64, 64, dg._binding.ctypes.byref(dg.Choice())))")
+    out = subprocess.run([sys.executable, "-c", code_bad], env=env, capture_output=True, text=True, check=True).stdout
+    assert out.strip() == "8"
