@@ -161,27 +161,31 @@ def run_gpu(args):
     R = args.reps
 
     cases = []        # (name, dict(meta), graph, weight_bytes_per_call)
+    keep = []         # every tensor a captured graph reads or writes stays alive with it
 
     def add(name, meta, calls, wbytes):
         with torch.cuda.stream(stream):
             g = _graph_case(torch, calls, R, stream)
         cases.append((name, meta, g, wbytes))
+        keep.append(calls)
 
     # --- the headline sweep
     sweep_cases = []
-    for (N, K) in SWEEP_NK:
+    only = None
+    if args.only:
+        only = tuple(int(v) for v in args.only.split(","))       # M,N,K
+    for (N, K) in SWEEP_NK if only is None else [(only[1], only[2])]:
         W0 = S.linear_inputs(1, N, K, device=dev)[1]
         wb = N * K * 2
         Ws = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)]
-        for M in SWEEP_M:
+        for M in SWEEP_M if only is None else [only[0]]:
             x = S.linear_inputs(M, N, K, device=dev)[0]
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K, device=dev)
             calls = [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Ws]
             add("gemv_bf16", {"M": M, "N": N, "K": K}, calls, wb)
             sweep_cases.append(len(cases) - 1)
-        del Ws, W0
-    if not args.sweep_only:
+    if not args.sweep_only and only is None:
         # --- GEMV 2048x1024 at M=1
         N, K = 2048, 1024
         x, W0 = S.linear_inputs(1, N, K, device=dev)
@@ -190,7 +194,7 @@ def run_gpu(args):
         y = torch.empty((1, N), dtype=torch.bfloat16, device=dev)
         ws = dg.workspace(dg.DG_OP_GEMV_BF16, 1, N, K, device=dev)
         add("gemv_bf16_2048x1024", {"M": 1, "N": N, "K": K},
-            [(lambda W=W: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Ws], wb)
+            [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Ws], wb)
         # --- gate/up
         Nh, K = 12288, 4096
         W0 = S.gate_up_inputs(1, Nh, K, device=dev)[1]
@@ -202,7 +206,6 @@ def run_gpu(args):
             ws = dg.workspace(dg.DG_OP_GATE_UP_SILU, M, Nh, K, device=dev)
             add("gate_up_silu", {"M": M, "N_half": Nh, "K": K},
                 [(lambda W=W, x=x, out=out, ws=ws: dg.dg_gate_up_silu(x, W, out, ws=ws, stream=stream)) for W in Ws], wb)
-        del Ws, W0
         # --- fp8 head
         x8, Wq, scale = S.head_inputs(8, HEAD_N, HEAD_K, device=dev)
         for M in HEAD_M:
@@ -211,7 +214,7 @@ def run_gpu(args):
             am = torch.empty((M,), dtype=torch.int32, device=dev)
             ws = dg.workspace(dg.DG_OP_HEAD_FP8_ARGMAX, M, HEAD_N, HEAD_K, device=dev)
             add("head_fp8_argmax", {"M": M, "N": HEAD_N, "K": HEAD_K},
-                [lambda x=x, logits=logits, am=am, ws=ws: dg.dg_head_fp8_argmax(
+                [lambda x=x, logits=logits, am=am, ws=ws, Wq=Wq, scale=scale: dg.dg_head_fp8_argmax(
                     x, Wq, scale, logits, am, ws=ws, stream=stream)], HEAD_N * HEAD_K + 4)
         # --- MoE
         W1q, s1, W2q, s2 = S.moe_weights(MOE_E, MOE_I, MOE_K, MOE_K, device=dev)
@@ -226,9 +229,11 @@ def run_gpu(args):
             b1 = u_mean * (2 * MOE_I * MOE_K + 2 * MOE_I * 4)
             b2 = u_mean * (MOE_K * MOE_I + MOE_K * 4)
             add("moe_w1_silu", {"M": M, "U_mean": u_mean},
-                [(lambda r=r: dg.dg_moe_w1_silu(r[0], r[1], W1q, s1, a, ws=ws1, stream=stream)) for r in routs], b1)
+                [(lambda r=r, a=a, ws1=ws1, W1q=W1q, s1=s1: dg.dg_moe_w1_silu(r[0], r[1], W1q, s1, a, ws=ws1, stream=stream))
+                 for r in routs], b1)
             add("moe_w2", {"M": M, "U_mean": u_mean},
-                [(lambda r=r: dg.dg_moe_w2(a, r[1], r[2], W2q, s2, yv, ws=ws2, stream=stream)) for r in routs], b2)
+                [(lambda r=r, a=a, yv=yv, ws2=ws2, W2q=W2q, s2=s2: dg.dg_moe_w2(a, r[1], r[2], W2q, s2, yv, ws=ws2, stream=stream))
+                 for r in routs], b2)
 
     n_cases = len(cases)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_cases)]
@@ -290,7 +295,7 @@ def run_gpu(args):
         ops.setdefault(s["op"], []).append(s)
 
     # ---- e2e through the public API with host buffers (x in, y out, pinned)
-    e2e = _e2e(torch, dg, S, dev, stream, args, l2)
+    e2e = _e2e(torch, dg, S, dev, stream, args, l2) if only is None else None
 
     launches = args.steps * R * n_cases
     res = {
@@ -309,7 +314,8 @@ def run_gpu(args):
         "config": {"workload": WORKLOAD, "calls_per_step": len(sweep),
                    "l2_defeat": f"weights rotate over >= 3x L2 ({l2 // 2**20} MiB) of copies inside "
                                 f"CUDA graphs of {R} calls",
-                   "parallelism": "replicas" if world > 1 else "single GPU"},
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "build_id": dg.dg_build_id()},
         "roofline": {"bound": "hbm", "achieved": round(value_rank, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(value_rank / peak, 4), "traffic": _traffic(dg),
                      "peak_source": peak_src, "kernel": "cc_dense_kernel (bf16 linear)",
@@ -458,6 +464,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep-only", action="store_true", help="only the headline sweep (no other ops)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="profiling: one sweep shape 'M,N,K' (no other ops, no e2e)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
