@@ -84,6 +84,7 @@ def lib():
     L.dg_gemv_bf16.argtypes = [P, P, P, I, I, I, P, Z, P, P]
     L.dg_gate_up_silu.argtypes = [P, P, P, I, I, I, P, Z, P, P]
     L.dg_head_fp8_argmax.argtypes = [P, P, P, P, P, I, I, I, P, Z, P, P]
+    L.dg_head_fp8_argmax_noalloc.argtypes = [P, P, P, P, P, I, I, I, P, P]
     L.dg_moe_w1_silu.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
     L.dg_moe_w2.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
     L.dg_select.argtypes = [I, I, I, I, ctypes.POINTER(Choice)]
@@ -98,7 +99,7 @@ def lib():
                                  ctypes.c_char_p, Z]
     L.dg_sweep.argtypes = [ctypes.POINTER(Shape), I, ctypes.c_char_p, I]
     for name in ("dg_init", "dg_device_status", "dg_device_status_clear", "dg_gemv_bf16",
-                 "dg_gate_up_silu", "dg_head_fp8_argmax", "dg_moe_w1_silu", "dg_moe_w2", "dg_select",
+                 "dg_gate_up_silu", "dg_head_fp8_argmax", "dg_head_fp8_argmax_noalloc", "dg_moe_w1_silu", "dg_moe_w2", "dg_select",
                  "dg_table_load", "dg_table_check", "dg_sweep"):
         getattr(L, name).restype = S
     _lib = L
@@ -204,6 +205,21 @@ def dg_head_fp8_argmax(x, Wq, scale, logits=None, argmax=None, ws=None, choice=N
     _ok(lib().dg_head_fp8_argmax(_ptr(x), _ptr(Wq), _ptr(scale), _ptr(logits), _ptr(argmax), M, N, K,
                                  _ptr(ws), ws.numel(), _stream(stream), _choice(choice)),
         "dg_head_fp8_argmax")
+    return logits, argmax
+
+
+def dg_head_fp8_argmax_noalloc(x, Wq, scale, logits=None, argmax=None, choice=None, stream=None,
+                               want_logits=True):
+    """dg_head_fp8_argmax with the library's static scratch instead of a workspace."""
+    M, K = x.shape
+    N = Wq.shape[0]
+    if logits is None and want_logits:
+        logits = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if argmax is None:
+        argmax = torch.empty((M,), dtype=torch.int32, device=x.device)
+    _check_dev(x, Wq, scale, logits, argmax)
+    _ok(lib().dg_head_fp8_argmax_noalloc(_ptr(x), _ptr(Wq), _ptr(scale), _ptr(logits), _ptr(argmax), M, N,
+                                         K, _stream(stream), _choice(choice)), "dg_head_fp8_argmax_noalloc")
     return logits, argmax
 
 

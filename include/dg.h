@@ -157,6 +157,26 @@ dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, 
                              int32_t* argmax, int M, int N, int K, void* ws, size_t ws_bytes,
                              dg_stream_t stream, const dg_choice* choice);
 
+/* The same head and pick for callers that cannot allocate device memory (no
+ * counterpart on the pages).  Engines whose device memory pool belongs to someone
+ * else, plugins whose host forbids device allocation, or code that runs after its
+ * memory budget is fixed cannot hand over a workspace; this entry point keeps the
+ * scratch (status word, pick ticket, per-CTA partials) in a static device array of
+ * 262,400 bytes inside the library instead, held by every GPU that loads the
+ * library until the process exits.  It calls no allocator.
+ * - Arguments and results as dg_head_fp8_argmax, without ws / ws_bytes.
+ * - The first call on a device looks up the array's device address (with that
+ *   device current); make that first call before any stream capture.
+ * - Each call clears the status word and ticket with an asynchronous memset on
+ *   `stream`, then launches.
+ * - All calls share the one array: calls that may overlap on the GPU (different
+ *   streams, or different host threads) race and must be serialised by the caller.
+ * - A launch that would need more than 4096 CTA partial slots (e.g. a choice with
+ *   tiny CTAs) is rejected with DG_ERR_WORKSPACE_TOO_SMALL and one stderr line. */
+dg_status dg_head_fp8_argmax_noalloc(const void* x, const void* Wq, const float* scale, void* logits,
+                                     int32_t* argmax, int M, int N, int K, dg_stream_t stream,
+                                     const dg_choice* choice);
+
 /* Routed-expert W1 with SiLU.mul, "Decode optimization round 3", "Retained
  * change 1: N-split W1/W2 MoE kernels" (experts split along N at small M).
  * A slot (t, k) is valid when 0 <= topk_ids[t, k] < E and no earlier slot of
