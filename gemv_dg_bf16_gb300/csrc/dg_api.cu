@@ -76,6 +76,10 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
     switch (op) {
     case DG_OP_GEMV_BF16:
     case DG_OP_GATE_UP_SILU:
+        if (M >= kTcMinRows) {
+            out->variant = DG_VAR_TC;      // dense enough for the tensor cores
+            break;
+        }
         out->params[0] = M <= 2 ? 4 : (M <= 4 ? 4 : 2);
         out->params[1] = 8;
         break;
@@ -170,12 +174,17 @@ size_t dg_workspace_bytes(dg_op op, int M, int N, int K, int topk)
     (void)K;
     size_t b = kWsData;
     switch (op) {
+    case DG_OP_GEMV_BF16:
+        if (M > 0 && N > 0 && K > 0) b = tc_workspace_bytes(M, N, K);
+        break;
+    case DG_OP_GATE_UP_SILU:
+        if (M > 0 && N > 0 && K > 0) b = tc_workspace_bytes(M, 2 * N, K);
+        break;
     case DG_OP_HEAD_FP8_ARGMAX:
         b += static_cast<size_t>(kMaxGrid) * 8 * 8;
         break;
     case DG_OP_MOE_W2:
-        if (M > 0 && topk > 0 && N > 0)
-            b += moe_terms_bytes(M, topk, N) + moe_ticket_bytes(M, N, 1);
+        if (M > 0 && topk > 0 && N > 0) b += moe_terms_bytes(M, topk, N);
         break;
     default:
         break;
@@ -300,6 +309,8 @@ dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int 
     if (!dev) return s;
     dg_choice c;
     if ((s = resolve_choice(DG_OP_GEMV_BF16, M, N, K, choice, &c)) != DG_OK) return s;
+    if (c.variant == DG_VAR_TC)
+        return launch_tc(false, dev, c, x, W, y, M, N, K, N, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
     if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
     DenseArgs a{};
     a.W = static_cast<const uint8_t*>(W);
@@ -325,6 +336,9 @@ dg_status dg_gate_up_silu(const void* x, const void* W_gu, void* out, int M, int
     if (!dev) return s;
     dg_choice c;
     if ((s = resolve_choice(DG_OP_GATE_UP_SILU, M, N_half, K, choice, &c)) != DG_OK) return s;
+    if (c.variant == DG_VAR_TC)
+        return launch_tc(true, dev, c, x, W_gu, out, M, 2 * N_half, K, N_half, ws, ws_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
     if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
     DenseArgs a{};
     a.W = static_cast<const uint8_t*>(W_gu);
@@ -375,8 +389,9 @@ static dg_status launch_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, 
     if (c.params[0] != 0 && c.params[0] != 4) return DG_ERR_BAD_VARIANT;
     if (wpc < 1 || wpc > 8 || c.params[2] < 0 || c.params[3] < 0) return DG_ERR_BAD_VARIANT;
     int tile = c.params[3];
-    if (tile == 0) tile = w1 ? wpc * 2 : wpc * 4;
+    if (tile == 0) tile = w1 ? wpc * 2 : (wpc * 4 < 32 ? 32 : wpc * 4);
     a.tile = tile;
+    if (!w1 && moe_tickets(a.M, a.Nout, tile) > kWsMaxCounters) return DG_ERR_BAD_VARIANT;
     const void* fn = w1 ? moe_w1_kernel() : moe_w2_kernel();
     const int threads = wpc * 32;
     const size_t smem = static_cast<size_t>(8) * a.K * 2;

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(256) moe_kernel(MoeArgs a)
     const int units = R.U * tiles;
     const int kv = a.K / 8;
     float* terms = reinterpret_cast<float*>(a.ws + kWsData);
-    unsigned* tickets = reinterpret_cast<unsigned*>(a.ws + kWsData + moe_terms_bytes(a.M, a.topk, a.Nout));
+    unsigned* tickets = reinterpret_cast<unsigned*>(a.ws + kWsCounters);
 
     if constexpr (W1) {
         // Invalid slots get a = 0 (no unit covers them).

@@ -24,10 +24,14 @@ namespace dg {
 constexpr int kSeg = 1024;                 // K elements per canonical segment
 constexpr unsigned kFull = 0xffffffffu;
 
-// Workspace layout (bytes from the start of ws).
+// Workspace layout (bytes from the start of ws).  Counters live in their own
+// region that no op uses for data, so one workspace may serve every op (calls
+// ordered on one stream); each op leaves its counters at zero when it finishes.
 constexpr size_t kWsStatus = 0;            // int32 sticky device status word
-constexpr size_t kWsTicket = 16;           // uint32 ticket of single-ticket kernels
-constexpr size_t kWsData = 256;            // per-op scratch starts here
+constexpr size_t kWsTicket = 16;           // uint32 ticket of single-ticket kernels (the head)
+constexpr size_t kWsCounters = 256;        // uint32 tickets of multi-ticket kernels (TC tiles, MoE)
+constexpr size_t kWsData = 32768;          // per-op scratch data starts here
+constexpr int kWsMaxCounters = static_cast<int>((kWsData - kWsCounters) / 4);
 
 __host__ __device__ constexpr int cpow2(int v) { int p = 1; while (p < v) p <<= 1; return p; }
 __host__ __device__ constexpr int clog2(int v) { int l = 0; while ((1 << l) < v) ++l; return l; }

@@ -19,6 +19,16 @@ const void* dense_kernel_head(int mt, int R);
 const void* moe_w1_kernel();
 const void* moe_w2_kernel();
 
+// tcgen05 family (dg_tc_dense.cu): padded token count, fixed K-split of a shape,
+// workspace bytes, and the launcher (bf16 linear or interleaved gate/up rows).
+int tc_mp(int M);
+int tc_nsplit(int N, int K, int M);
+size_t tc_workspace_bytes(int M, int N, int K);
+
+struct DeviceInfo;
+dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W,
+                    void* out, int M, int N, int K, int ld_out, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 struct DeviceInfo {
     int device = -1;
     int sm_count = 0;
@@ -39,6 +49,9 @@ int occupancy(const void* fn, int threads, size_t smem);
 constexpr size_t kMaxDynSmem = 200 * 1024;
 // Budget for staged activations of the dense CUDA-core family.
 constexpr size_t kXsBudget = 96 * 1024;
+
+// Smallest row bucket the bf16 linear and gate/up send to the tensor cores.
+constexpr int kTcMinRows = 6;
 
 // Compiled default choice for (op, M, N, K).
 void default_choice(dg_op op, int M, int N, int K, dg_choice* out);

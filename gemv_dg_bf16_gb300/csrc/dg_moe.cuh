@@ -23,10 +23,9 @@ __host__ __device__ inline size_t moe_terms_bytes(int M, int topk, int Nout)
     return (static_cast<size_t>(M) * topk * Nout * 4 + 255) / 256 * 256;
 }
 
-__host__ __device__ inline size_t moe_ticket_bytes(int M, int Nout, int tile)
+__host__ __device__ inline int moe_tickets(int M, int Nout, int tile)
 {
-    const int tiles = (Nout + tile - 1) / tile;
-    return (static_cast<size_t>(M) * tiles * 4 + 255) / 256 * 256;
+    return M * ((Nout + tile - 1) / tile);
 }
 
 }  // namespace dg

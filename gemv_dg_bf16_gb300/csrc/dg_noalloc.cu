@@ -17,7 +17,8 @@
 
 namespace {
 
-// 256 bytes of header (status word, ticket) + partials for up to 4096 CTAs x 8 rows: exactly
+// The workspace header (status word, ticket, counter region) + partials for up to
+// 4096 CTAs x 8 rows: exactly
 // dg_workspace_bytes(DG_OP_HEAD_FP8_ARGMAX, ...), which the head checks its workspace against.
 constexpr size_t kNoAllocMaxCtas = 4096;
 constexpr size_t kNoAllocBytes = dg::kWsData + kNoAllocMaxCtas * 8 * 8;

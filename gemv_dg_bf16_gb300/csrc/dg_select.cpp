@@ -184,6 +184,13 @@ bool valid_bucket(int m)
 // Returns "" when the choice is acceptable for the op, else the reason.
 std::string check_choice(int op, const dg_choice& c)
 {
+    if (c.variant == DG_VAR_TC) {
+        if (op != DG_OP_GEMV_BF16 && op != DG_OP_GATE_UP_SILU) return "no tensor-core variant for this op";
+        if (c.params[0] != 0 && (c.params[0] < 2 || c.params[0] > 8)) return "pipeline stages must be 2..8";
+        for (int i = 1; i < 6; ++i)
+            if (c.params[i] != 0) return "unused tensor-core parameter set";
+        return "";
+    }
     if (c.variant != DG_VAR_CC_WARP) return "variant not in this build's selection space";
     const int R = c.params[0], wpc = c.params[1];
     if (op == DG_OP_MOE_W1 || op == DG_OP_MOE_W2) {
@@ -358,7 +365,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 1; }
+int dg_selection_space(void) { return 2; }
 
 const char* dg_build_id(void) { return build_id(); }
 

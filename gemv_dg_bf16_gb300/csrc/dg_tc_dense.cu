@@ -1,0 +1,481 @@
+// dg_tc_dense.cu -- tcgen05 tensor-core family (DG_VAR_TC) for the bf16 linear and
+// the fused gate/up + SiLU.mul at M >= 16 (here the contraction is dense enough
+// that CUDA-core FMA throughput, not HBM, would bound it).
+//
+// Swap-AB: a CTA owns a tile of 128 weight rows (the MMA's M) and one fixed K
+// range; the tokens are the MMA's N (M padded to MP in {16, 32, 64, 128}), so
+// D[128, MP] = W_tile[128, Kr] . x[MP, Kr]^T accumulates in TMEM (fp32).
+//   warp 0      TMA producer: 128x64 weight box + MPx64 activation box per stage
+//               (128-byte swizzle), into a ring of `stages` shared-memory slots
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (4 x K=16 per stage),
+//               commits each stage back to its "empty" barrier and the last one
+//               to the accumulator barrier
+//   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
+//               32*(w%4)..+31), then store / pair gate+up / write a K-split partial
+// Canonical order of this family: the K range of a tile is cut into `nsplit`
+// contiguous ranges of 64-element blocks, a fixed function of (N, K, MP)
+// (tc_nsplit below); each range is one MMA chain from zero in ascending k; the
+// range partials are folded left in fp32.  The nsplit CTAs of a tile form one
+// thread-block cluster: each parks its fp32 partial tile in its own shared
+// memory, and after a cluster barrier each CTA folds a slice of the tile's rows
+// by reading every rank's partial through distributed shared memory, in rank
+// order.  Variants (pipeline depth) change no bits.
+// Every mbarrier wait is bounded: on timeout the kernel flags
+// DG_DEVERR_WAIT_TIMEOUT in the workspace status word and winds down.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "dg_common.cuh"
+#include "dg_internal.h"
+
+namespace dg {
+namespace {
+
+constexpr int kTileRows = 128;                    // MMA M
+constexpr int kKB = 64;                           // K per stage: one 128-byte swizzled row
+constexpr int kWBox = kTileRows * kKB * 2;        // 16 KB
+constexpr int kThreads = 192;
+constexpr int kMaxCluster = 8;                    // portable thread-block cluster size
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s bound on any wait
+
+struct TcArgs {
+    int N, K, M;
+    int nsplit, nkb, tiles;
+    int stages;
+    uint16_t* out;
+    int ld_out;
+    uint8_t* ws;          // status word only (the K-split fold stays on chip)
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; returns false (and raises the CTA's abort flag) on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag)
+{
+    if (mbar_try(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitNs) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
+// groups 1024 bytes apart (stride byte offset), descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;              // leading byte offset (unused for this layout)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;       // stride byte offset
+    d |= static_cast<uint64_t>(1) << 46;               // version
+    d |= static_cast<uint64_t>(2) << 61;               // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major,
+// N = mp, M = 128.
+__host__ __device__ constexpr uint32_t mma_idesc(int mp)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(mp >> 3) << 17) |
+           (static_cast<uint32_t>(kTileRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+
+// Every thread of every CTA of the cluster executes this, unconditionally.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Final value of (row n, token t) -> output.  Gate/up: even rows are gate rows,
+// odd rows up rows; lanes hold consecutive rows, so the up value is one lane up.
+template <int EPI>
+__device__ __forceinline__ void emit(const TcArgs& a, int t, int n, float v, bool valid)
+{
+    if constexpr (EPI == 0) {
+        if (valid) a.out[static_cast<size_t>(t) * a.ld_out + n] = f32_to_bf16_bits(v);
+    } else {
+        const float u = __shfl_down_sync(kFull, v, 1);
+        if (valid && (n % 2) == 0) {
+            const float silu = v / (1.0f + expf(-v));
+            a.out[static_cast<size_t>(t) * a.ld_out + n / 2] = f32_to_bf16_bits(silu * u);
+        }
+    }
+}
+
+template <int MP, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_dense_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a)
+{
+    constexpr int kXBox = MP * kKB * 2;
+    constexpr int kStage = kWBox + kXBox;
+    constexpr uint32_t kCols = MP < 32 ? 32 : MP;
+    constexpr uint32_t kIdesc = mma_idesc(MP);
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = a.stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kStage);   // full[S], empty[S], accum
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool clustered = a.nsplit > 1;
+    const int tile = blockIdx.x / a.nsplit;
+    const int split = clustered ? static_cast<int>(cluster_rank()) : 0;
+    const int kb0 = static_cast<int>((static_cast<long long>(split) * a.nkb) / a.nsplit);
+    const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * a.nkb) / a.nsplit);
+    const int nkb = kb1 - kb0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2 * S + 1; ++s) mbar_init(smem_u32(bars + s), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                     "r"(kCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (clustered) cluster_sync_all();     // every rank's barriers exist before any remote access
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t tmem = *tmem_holder;
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), accum = smem_u32(bars + 2 * S);
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % S;
+                const uint32_t round = static_cast<uint32_t>(i / S);
+                if (!mbar_wait(empty0 + 8 * s, (round & 1u) ^ 1u, abort_flag)) break;
+                const uint32_t dst = smem_u32(smem + s * kStage);
+                mbar_expect_tx(full0 + 8 * s, kStage);
+                const int k = (kb0 + i) * kKB;
+                tma_load_2d(dst, &tmW, k, tile * kTileRows, full0 + 8 * s);
+                tma_load_2d(dst + kWBox, &tmX, k, 0, full0 + 8 * s);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            for (int i = 0; i < nkb; ++i) {
+                const int s = i % S;
+                const uint32_t round = static_cast<uint32_t>(i / S);
+                if (!mbar_wait(full0 + 8 * s, round & 1u, abort_flag)) break;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t wa = smem_u32(smem + s * kStage), xa = wa + kWBox;
+#pragma unroll
+                for (int kk = 0; kk < kKB / 16; ++kk)
+                    mma_bf16(tmem, smem_desc(wa + kk * 32), smem_desc(xa + kk * 32), kIdesc,
+                             (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(empty0 + 8 * s);
+            }
+            mma_commit(accum);           // fires once every MMA issued above has completed
+        }
+    } else {
+        // Epilogue warps 2..5 -> TMEM lane quarter (warp % 4).
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const int n = tile * kTileRows + row;
+        const bool ok = mbar_wait(accum, 0, abort_flag);
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        if (!ok || *abort_flag) {
+            if (row == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
+        } else if (!clustered) {
+#pragma unroll 1
+            for (int c = 0; c < MP / 16; ++c) {
+                uint32_t v[16];
+                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int t = c * 16 + j;
+                    emit<EPI>(a, t, n, __uint_as_float(v[j]), t < a.M && n < a.N);
+                }
+            }
+        } else {
+            // Park this rank's partial tile P[t][row] (fp32) in the now idle stage memory.
+            float* P = reinterpret_cast<float*>(smem);
+#pragma unroll 1
+            for (int c = 0; c < MP / 16; ++c) {
+                uint32_t v[16];
+                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) P[(c * 16 + j) * kTileRows + row] = __uint_as_float(v[j]);
+            }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    }
+    if (clustered) {
+        cluster_sync_all();                  // every rank's partial tile is in place
+        if (warp >= 2) {
+            // This rank folds rows [lo, hi) (even bounds keep gate/up pairs together)
+            // for all tokens: P_0 + P_1 + ... in rank order, read through DSMEM.
+            const int etid = threadIdx.x - 64;
+            const int lo = (split * (kTileRows / 2) / a.nsplit) * 2;
+            const int hi = ((split + 1) * (kTileRows / 2) / a.nsplit) * 2;
+            const int w = hi - lo;
+            const int count = w * a.M;
+            const uint32_t pbase = smem_u32(smem);
+            const bool live = !*abort_flag;
+            for (int base = 0; base < count; base += 128) {
+                const int e = base + etid;
+                const bool valid = e < count && live;
+                const int t = valid ? e / w : 0;
+                const int r = valid ? lo + (e - t * w) : lo;
+                float y = 0.0f;
+                if (valid) {
+                    const uint32_t off = static_cast<uint32_t>((t * kTileRows + r) * 4);
+                    y = ld_dsmem_f32(map_to_rank(pbase + off, 0));
+                    for (int s2 = 1; s2 < a.nsplit; ++s2) y = y + ld_dsmem_f32(map_to_rank(pbase + off, s2));
+                }
+                const int n2 = tile * kTileRows + r;
+                emit<EPI>(a, t, n2, y, valid && n2 < a.N);
+            }
+        }
+        cluster_sync_all();                  // no rank leaves while others still read its partials
+    }
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
+    if (warp == 1) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols));
+    }
+}
+
+// ------------------------------------------------------------------------ host
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
+               uint32_t box_outer)
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        cudaGetLastError();
+    });
+    if (!g_encode) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MP, int EPI>
+const void* tc_fn()
+{
+    return reinterpret_cast<const void*>(&tc_dense_kernel<MP, EPI>);
+}
+
+const void* tc_lookup(int mp, int epi)
+{
+    switch (mp * 2 + epi) {
+    case 16 * 2 + 0: return tc_fn<16, 0>();
+    case 16 * 2 + 1: return tc_fn<16, 1>();
+    case 32 * 2 + 0: return tc_fn<32, 0>();
+    case 32 * 2 + 1: return tc_fn<32, 1>();
+    case 64 * 2 + 0: return tc_fn<64, 0>();
+    case 64 * 2 + 1: return tc_fn<64, 1>();
+    case 128 * 2 + 0: return tc_fn<128, 0>();
+    case 128 * 2 + 1: return tc_fn<128, 1>();
+    default: return nullptr;
+    }
+}
+
+int default_stages(int mp)
+{
+    // Two CTAs per SM: about 100 KB of shared memory each.
+    return mp <= 32 ? 5 : (mp <= 64 ? 4 : 3);
+}
+
+}  // namespace
+
+int tc_mp(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
+
+int tc_nsplit(int N, int K, int M)
+{
+    const int tiles = (N + kTileRows - 1) / kTileRows;
+    const int nkb = (K + kKB - 1) / kKB;
+    (void)M;
+    int ns = (160 + tiles - 1) / tiles;
+    if (ns > kMaxCluster) ns = kMaxCluster;
+    if (ns > nkb) ns = nkb;
+    if (ns < 1) ns = 1;
+    return ns;
+}
+
+size_t tc_workspace_bytes(int M, int N, int K)
+{
+    const int tiles = (N + kTileRows - 1) / kTileRows;
+    const int ns = tc_nsplit(N, K, M);
+    (void)tiles;
+    (void)ns;
+    return kWsData;
+}
+
+dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W,
+                    void* out, int M, int N, int K, int ld_out, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    (void)dev;
+    if (M < 1 || M > 128) return DG_ERR_UNSUPPORTED_SHAPE;
+    const int mp = tc_mp(M);
+    const int epi = gate_up ? 1 : 0;
+    const void* fn = tc_lookup(mp, epi);
+    if (!fn) return DG_ERR_BAD_VARIANT;
+    int stages = c.params[0] > 0 ? c.params[0] : default_stages(mp);
+    if (stages < 2 || stages > 8) return DG_ERR_BAD_VARIANT;
+    const size_t stage_bytes = kWBox + static_cast<size_t>(mp) * kKB * 2;
+    const size_t smem = 1024 + stages * stage_bytes + (2 * stages + 1) * 8 + 16;
+    if (smem > kMaxDynSmem) return DG_ERR_BAD_VARIANT;
+    if (ws_bytes < tc_workspace_bytes(M, N, K)) return DG_ERR_WORKSPACE_TOO_SMALL;
+    TcArgs a{};
+    a.N = N;
+    a.K = K;
+    a.M = M;
+    a.tiles = (N + kTileRows - 1) / kTileRows;
+    a.nkb = (K + kKB - 1) / kKB;
+    a.nsplit = tc_nsplit(N, K, M);
+    const size_t part_bytes = static_cast<size_t>(mp) * kTileRows * 4;
+    if (a.nsplit > 1 && part_bytes > static_cast<size_t>(stages) * stage_bytes) return DG_ERR_BAD_VARIANT;
+    a.stages = stages;
+    a.out = static_cast<uint16_t*>(out);
+    a.ld_out = ld_out;
+    a.ws = static_cast<uint8_t*>(ws);
+    CUtensorMap tmW, tmX;
+    if (!encode_2d(&tmW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kKB, kTileRows) ||
+        !encode_2d(&tmX, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kKB, static_cast<uint32_t>(mp)))
+        return DG_ERR_CUDA;
+    if (occupancy(fn, kThreads, smem) < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+    void* args[] = {&tmW, &tmX, &a};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.tiles * a.nsplit));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.nsplit);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+        cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    return DG_OK;
+}
+
+}  // namespace dg

@@ -162,7 +162,7 @@ dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, 
  * else, plugins whose host forbids device allocation, or code that runs after its
  * memory budget is fixed cannot hand over a workspace; this entry point keeps the
  * scratch (status word, pick ticket, per-CTA partials) in a static device array of
- * 262,400 bytes inside the library instead, held by every GPU that loads the
+ * 294,912 bytes inside the library instead, held by every GPU that loads the
  * library until the process exits.  It calls no allocator.
  * - Arguments and results as dg_head_fp8_argmax, without ws / ws_bytes.
  * - The first call on a device looks up the array's device address (with that

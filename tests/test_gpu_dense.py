@@ -27,13 +27,21 @@ def _lin_check(x, W, y, rows=None):
     assert (exc <= 0).all(), f"max excess {exc.max():.3e} at {np.unravel_index(exc.argmax(), exc.shape)}"
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 2048, 1024), (3, 130, 1040), (5, 77, 520), (8, 300, 2056),
-                                   (16, 96, 264), (37, 65, 136), (128, 64, 1024), (2, 1, 8)])
-def test_gemv_small_exhaustive(cuda_device, M, N, K):
+CC = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0)
+TC = dg.Choice.make(dg.DG_VAR_TC, 0)
+SMALL = [(1, 2048, 1024), (3, 130, 1040), (5, 77, 520), (8, 300, 2056), (16, 96, 264), (37, 65, 136),
+         (128, 64, 1024), (2, 1, 8), (16, 1000, 4096), (64, 300, 3000), (100, 257, 1096), (128, 640, 6144)]
+
+
+@pytest.mark.parametrize("family", ["cc", "tc", "default"])
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_gemv_small_exhaustive(cuda_device, M, N, K, family):
     x, W = S.linear_inputs(M, N, K, device=cuda_device)
-    y = dg.dg_gemv_bf16(x, W)
+    ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K)
+    y = dg.dg_gemv_bf16(x, W, ws=ws, choice={"cc": CC, "tc": TC, "default": None}[family])
     torch.cuda.synchronize()
     _lin_check(x, W, y)
+    assert dg.dg_device_status(ws) == 0
 
 
 @pytest.mark.parametrize("N,K", SWEEP_NK)
@@ -55,25 +63,46 @@ def _variants(op, mt_max):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1000, 3080), (3, 515, 1024), (8, 256, 4096), (13, 70, 2048)])
-def test_gemv_variants_bitwise_identical(cuda_device, M, N, K):
+def test_gemv_cc_variants_bitwise_identical(cuda_device, M, N, K):
     x, W = S.linear_inputs(M, N, K, device=cuda_device)
-    ref = dg.dg_gemv_bf16(x, W)
+    ref = dg.dg_gemv_bf16(x, W, choice=CC)
     for c in _variants(dg.DG_OP_GEMV_BF16, 8):
         y = dg.dg_gemv_bf16(x, W, choice=c)
         assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), repr(c)
     for _ in range(3):
-        assert torch.equal(dg.dg_gemv_bf16(x, W).view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(dg.dg_gemv_bf16(x, W, choice=CC).view(torch.int16), ref.view(torch.int16))
 
 
-def test_gemv_identity_and_one_hot_exact(cuda_device):
+@pytest.mark.parametrize("M,N,K", [(16, 4096, 4096), (40, 1000, 3080), (128, 768, 2048), (6, 32768, 1024)])
+def test_gemv_tc_variants_bitwise_identical(cuda_device, M, N, K):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K)
+    ref = dg.dg_gemv_bf16(x, W, ws=ws, choice=TC)
+    for st in (2, 3, 4, 5, 6):
+        c = dg.Choice.make(dg.DG_VAR_TC, st)
+        try:
+            y = dg.dg_gemv_bf16(x, W, ws=ws, choice=c)
+        except dg.DGError as e:            # a depth that does not fit shared memory for this M
+            assert e.status == 8
+            continue
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), st
+    for _ in range(3):
+        assert torch.equal(dg.dg_gemv_bf16(x, W, ws=ws, choice=TC).view(torch.int16), ref.view(torch.int16))
+    assert dg.dg_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("family", ["cc", "tc"])
+def test_gemv_identity_and_one_hot_exact(cuda_device, family):
+    c = {"cc": CC, "tc": TC}[family]
     K = 1040
     eye = torch.eye(K, dtype=torch.bfloat16, device=cuda_device)
-    x, W = S.linear_inputs(5, 300, K, device=cuda_device)
-    assert torch.equal(dg.dg_gemv_bf16(x, eye).view(torch.int16), x.view(torch.int16))
+    for M in (5, 40):
+        x, W = S.linear_inputs(M, 300, K, device=cuda_device)
+        assert torch.equal(dg.dg_gemv_bf16(x, eye, choice=c).view(torch.int16), x.view(torch.int16))
     for k in (0, 517, K - 1):
         e = torch.zeros((1, K), dtype=torch.bfloat16, device=cuda_device)
         e[0, k] = 1.0
-        y = dg.dg_gemv_bf16(e, W)
+        y = dg.dg_gemv_bf16(e, W, choice=c)
         assert torch.equal(y[0].view(torch.int16), W[:, k].contiguous().view(torch.int16))
 
 
@@ -104,10 +133,12 @@ def _gate_up_check(x, Wgu, out, cols=None):
     assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
 
 
-@pytest.mark.parametrize("M,Nh,K", [(1, 96, 1024), (3, 65, 1040), (6, 200, 520), (12, 33, 2048), (64, 16, 264)])
-def test_gate_up_small_exhaustive(cuda_device, M, Nh, K):
+@pytest.mark.parametrize("family", ["cc", "tc", "default"])
+@pytest.mark.parametrize("M,Nh,K", [(1, 96, 1024), (3, 65, 1040), (6, 200, 520), (12, 33, 2048), (64, 16, 264),
+                                    (16, 700, 4096), (128, 96, 1544)])
+def test_gate_up_small_exhaustive(cuda_device, M, Nh, K, family):
     x, Wgu = S.gate_up_inputs(M, Nh, K, device=cuda_device)
-    out = dg.dg_gate_up_silu(x, Wgu)
+    out = dg.dg_gate_up_silu(x, Wgu, choice={"cc": CC, "tc": TC, "default": None}[family])
     torch.cuda.synchronize()
     _gate_up_check(x, Wgu, out)
 
@@ -122,10 +153,15 @@ def test_gate_up_full_size_sampled(cuda_device, M):
 
 def test_gate_up_variants_bitwise_identical(cuda_device):
     x, Wgu = S.gate_up_inputs(6, 300, 2056, device=cuda_device)
-    ref = dg.dg_gate_up_silu(x, Wgu)
+    ref = dg.dg_gate_up_silu(x, Wgu, choice=CC)
     for c in _variants(dg.DG_OP_GATE_UP_SILU, 8):
         out = dg.dg_gate_up_silu(x, Wgu, choice=c)
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), repr(c)
+    x, Wgu = S.gate_up_inputs(32, 3000, 4096, device=cuda_device)
+    ref = dg.dg_gate_up_silu(x, Wgu, choice=TC)
+    for st in (2, 3, 4, 5):
+        out = dg.dg_gate_up_silu(x, Wgu, choice=dg.Choice.make(dg.DG_VAR_TC, st))
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), st
 
 
 def test_gate_up_matches_two_linears_plus_silu_on_device(cuda_device):
@@ -136,11 +172,12 @@ def test_gate_up_matches_two_linears_plus_silu_on_device(cuda_device):
         Wf[2 * j, j] = 1.0
         Wf[2 * j + 1, 32 + j] = 1.0
     x = torch.randn((2, K), generator=torch.Generator().manual_seed(3)).to(torch.bfloat16)
-    out = dg.dg_gate_up_silu(x.to(cuda_device), Wf.to(torch.bfloat16).to(cuda_device))
     g = x.float()[:, :Nh]
     u = x.float()[:, 32:32 + Nh]
     ref = (g / (1 + torch.exp(-g)) * u)
-    assert torch.allclose(out.float().cpu(), ref, rtol=2 ** -7, atol=1e-6)
+    for c in (CC, TC):
+        out = dg.dg_gate_up_silu(x.to(cuda_device), Wf.to(torch.bfloat16).to(cuda_device), choice=c)
+        assert torch.allclose(out.float().cpu(), ref, rtol=2 ** -7, atol=1e-6)
 
 
 # ---------------------------------------------------------------- argument errors on device
