@@ -319,8 +319,9 @@ def run_gpu(args):
         "roofline": {"bound": "hbm", "achieved": round(value_rank, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(value_rank / peak, 4), "traffic": _traffic(dg),
                      "peak_source": peak_src, "kernel": "cc_dense_kernel (bf16 linear)",
-                     "frac_m_le_16": round(sum(s["weight_bytes"] for s in small) /
-                                           (sum(s["us"] for s in small) * 1e-6) / 1e9 / peak, 4)},
+                     "frac_m_le_16": (round(sum(s["weight_bytes"] for s in small) /
+                                            (sum(s["us"] for s in small) * 1e-6) / 1e9 / peak, 4)
+                                      if small else None)},
         "clocks": clk,
         "e2e": e2e,
         "gpu_launches": launches,

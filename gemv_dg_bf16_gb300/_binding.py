@@ -49,7 +49,7 @@ class Choice(ctypes.Structure):
 
 class Shape(ctypes.Structure):
     _fields_ = [("op", ctypes.c_int32), ("M", ctypes.c_int32), ("N", ctypes.c_int32),
-                ("K", ctypes.c_int32), ("topk", ctypes.c_int32)]
+                ("K", ctypes.c_int32), ("topk", ctypes.c_int32), ("E", ctypes.c_int32)]
 
 
 class DGError(RuntimeError):
@@ -289,6 +289,6 @@ def dg_table_check(path: str, arch: str, driver_version: int, runtime_version: i
 
 
 def dg_sweep(shapes, out_path: str, reps: int = 20):
-    """shapes: iterable of (op, M, N, K, topk)."""
+    """shapes: iterable of (op, M, N, K, topk[, E]); writes the shape table JSON to out_path."""
     arr = (Shape * len(shapes))(*[Shape(*s) for s in shapes])
     _ok(lib().dg_sweep(arr, len(shapes), out_path.encode(), reps), "dg_sweep")

@@ -237,17 +237,24 @@ int dg_selection_space(void);
 dg_status dg_table_check(const char* path, const char* arch, int driver_version,
                          int runtime_version, int* entries, char* reason, size_t reason_cap);
 
-/* On-device sweep: for every op and shape in the request list, time every
- * candidate variant, byte-compare its output with the default variant's and
- * write a table that keeps every candidate's time and parameters beside the
- * pick; a candidate replaces the default only if it is bitwise equal and at
- * least 2 % faster.  mstar PR #1104, "What changed" (the promotion rule);
- * Strata PR #1297, "Summary" and "True-default baseline".
- * `shapes` is an array of n_shapes records {op, M, N, K, topk}; the sweep
- * allocates and frees its own scratch buffers (it is an offline tool, not a
- * decode-loop call).  Writes the JSON table to out_path. */
+/* On-device sweep: for every shape in the request list, time every candidate
+ * variant of the bucket's kernel family the way the benchmark does (CUDA graphs
+ * of back-to-back calls over weight copies that exceed the L2 cache), byte-compare
+ * each candidate's output with the compiled default's on the same inputs, and
+ * write a table that keeps every candidate's time and parameters beside the pick.
+ * A candidate replaces the default only if it is bitwise equal and at least 2 %
+ * faster.  mstar PR #1104, "What changed" (the promotion rule, every candidate's
+ * time kept beside the choice); Strata PR #1297, "Summary" (byte-compared
+ * variants only) and "True-default baseline"; "Decode optimization round 3",
+ * "Rejected paths" (re-measure every row against the incumbent in context).
+ * Each record names the op and its sizes as dg_workspace_bytes does (N = N_half
+ * for gate/up, N = I and K = hidden for MoE W1, N = Nout and K = I for MoE W2);
+ * E is the expert count (0 = 128).  The table is written to out_path as JSON with
+ * this build's identity.  The sweep allocates and frees its own device buffers
+ * (it is an offline tool, not a decode-loop call) and synchronises the device.
+ * Returns the first error met; shapes after it are not measured. */
 typedef struct {
-    int32_t op, M, N, K, topk;
+    int32_t op, M, N, K, topk, E;
 } dg_shape;
 dg_status dg_sweep(const dg_shape* shapes, int n_shapes, const char* out_path, int reps);
 

@@ -1,0 +1,84 @@
+"""On-device sweep -> shape table -> selector, on a GPU.
+
+The sweep keeps every candidate's time beside the pick, promotes only bitwise-equal
+candidates at least 2 % faster than the default, and a loaded table drives dg_select;
+results through an engaged table equal the default's bits.
+"""
+import json
+
+import pytest
+import torch
+
+import gemv_dg_bf16_gb300 as dg
+from synth import decode_inputs as S
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [
+    (dg.DG_OP_GEMV_BF16, 1, 2048, 1024, 0, 0),
+    (dg.DG_OP_GEMV_BF16, 16, 4096, 1024, 0, 0),
+    (dg.DG_OP_GATE_UP_SILU, 2, 1024, 1024, 0, 0),
+    (dg.DG_OP_HEAD_FP8_ARGMAX, 1, 8192, 1024, 0, 0),
+    (dg.DG_OP_MOE_W1, 2, 256, 512, 6, 16),
+    (dg.DG_OP_MOE_W2, 2, 512, 256, 6, 16),
+]
+
+
+@pytest.fixture(scope="module")
+def table(tmp_path_factory, cuda_device):
+    path = str(tmp_path_factory.mktemp("tab") / "table.json")
+    dg.dg_sweep(SHAPES, path, reps=5)
+    with open(path) as f:
+        return path, json.load(f)
+
+
+def test_sweep_table_contents(table):
+    path, doc = table
+    assert doc["format"] == "libdecodegemm-table"
+    assert doc["identity"]["selection_space"] == dg.dg_selection_space()
+    assert doc["identity"]["build"] == dg.dg_build_id()
+    assert len(doc["entries"]) == len(SHAPES)
+    for e in doc["entries"]:
+        cands = e["candidates"]
+        assert len(cands) >= 2                               # every candidate kept beside the pick
+        assert all(c["us"] > 0 for c in cands)
+        d = [c for c in cands if c["variant"] == e["default"]["variant"] and c["params"] == e["default"]["params"]]
+        assert d and d[0]["bitwise"]
+        pk = [c for c in cands if c["variant"] == e["pick"]["variant"] and c["params"] == e["pick"]["params"]]
+        assert pk and pk[0]["bitwise"]                       # only byte-identical candidates are picked
+        if e["pick"] != e["default"]:
+            assert e["pick_us"] <= 0.98 * e["default_us"]    # the 2 % promotion floor
+        fams = {c["variant"] for c in cands}
+        assert len(fams) == 1                                # one kernel family per bucket
+
+
+def test_engaged_table_drives_select_and_keeps_bits(table, cuda_device):
+    path, doc = table
+    M, N, K = 16, 4096, 1024
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    ref = dg.dg_gemv_bf16(x, W)                              # compiled default
+    dg.dg_table_load(path)
+    try:
+        assert dg.dg_table_entries() == len(SHAPES)
+        c = dg.dg_select(dg.DG_OP_GEMV_BF16, 13, N, K)       # 13 pads up to the 16 bucket
+        assert c.from_table == 1
+        ent = [e for e in doc["entries"] if e["op"] == "gemv_bf16" and e["M"] == 16][0]
+        assert [c.variant, list(c.params)] == [ent["pick"]["variant"], ent["pick"]["params"]]
+        y = dg.dg_gemv_bf16(x, W)
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
+        assert dg.dg_select(dg.DG_OP_GEMV_BF16, 16, 4096, 4096).from_table == 0   # no nearest-size fallback
+    finally:
+        dg.dg_table_clear()
+    assert dg.dg_table_entries() == 0
+
+
+def test_stale_table_refused_on_device(table, tmp_path, cuda_device):
+    path, doc = table
+    doc = dict(doc)
+    doc["identity"] = dict(doc["identity"], selection_space=99)
+    bad = tmp_path / "stale.json"
+    bad.write_text(json.dumps(doc))
+    with pytest.raises(dg.DGError) as e:
+        dg.dg_table_load(str(bad))
+    assert e.value.status == 6
+    assert dg.dg_table_entries() == 0
