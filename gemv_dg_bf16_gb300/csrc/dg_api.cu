@@ -69,20 +69,22 @@ int occupancy(const void* fn, int threads, size_t smem)
 
 void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
 {
-    (void)N;
     (void)K;
     std::memset(out, 0, sizeof *out);
     out->variant = DG_VAR_CC_WARP;
     switch (op) {
     case DG_OP_GEMV_BF16:
-    case DG_OP_GATE_UP_SILU:
+    case DG_OP_GATE_UP_SILU: {
         if (M >= kTcMinRows) {
             out->variant = DG_VAR_TC;      // dense enough for the tensor cores
             break;
         }
-        out->params[0] = M <= 2 ? 4 : (M <= 4 ? 4 : 2);
+        // Enough 8-warp CTAs to put two on every SM of a 152-SM part.
+        const long rows = op == DG_OP_GATE_UP_SILU ? 2L * N : static_cast<long>(N);
+        out->params[0] = rows >= 304L * 32 ? 4 : (rows >= 304L * 16 ? 2 : (op == DG_OP_GATE_UP_SILU ? 2 : 1));
         out->params[1] = 8;
         break;
+    }
     case DG_OP_HEAD_FP8_ARGMAX:
         out->params[0] = M <= 2 ? 8 : (M <= 4 ? 4 : 4);
         out->params[1] = 8;

@@ -182,10 +182,12 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t ra
     return r;
 }
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr)
+// Four consecutive fp32 from a cluster peer's shared memory (read after a cluster
+// barrier; the data does not change afterwards, so loads may be freely reordered).
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr)
 {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    float4 v;
+    asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
     return v;
 }
 
@@ -202,6 +204,31 @@ __device__ __forceinline__ void emit(const TcArgs& a, int t, int n, float v, boo
             const float silu = v / (1.0f + expf(-v));
             a.out[static_cast<size_t>(t) * a.ld_out + n / 2] = f32_to_bf16_bits(silu * u);
         }
+    }
+}
+
+// Four consecutive rows n..n+3 of token t held by one thread (n a multiple of 4).
+template <int EPI>
+__device__ __forceinline__ void emit4(const TcArgs& a, int t, int n, float4 v)
+{
+    if constexpr (EPI == 0) {
+        uint16_t* dst = a.out + static_cast<size_t>(t) * a.ld_out + n;
+        if (n + 3 < a.N && (a.ld_out % 4) == 0) {
+            const uint32_t lo = f32_to_bf16_bits(v.x) | (static_cast<uint32_t>(f32_to_bf16_bits(v.y)) << 16);
+            const uint32_t hi = f32_to_bf16_bits(v.z) | (static_cast<uint32_t>(f32_to_bf16_bits(v.w)) << 16);
+            *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+        } else {
+            const float f[4] = {v.x, v.y, v.z, v.w};
+            for (int i = 0; i < 4; ++i)
+                if (n + i < a.N) dst[i] = f32_to_bf16_bits(f[i]);
+        }
+    } else {
+        // rows (n, n+1) and (n+2, n+3) are (gate, up) pairs of outputs n/2 and n/2 + 1
+        const float s0 = v.x / (1.0f + expf(-v.x));
+        const float s1 = v.z / (1.0f + expf(-v.z));
+        uint16_t* dst = a.out + static_cast<size_t>(t) * a.ld_out + n / 2;
+        if (n + 1 < a.N) dst[0] = f32_to_bf16_bits(s0 * v.y);
+        if (n + 3 < a.N) dst[1] = f32_to_bf16_bits(s1 * v.w);
     }
 }
 
@@ -312,28 +339,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (clustered) {
         cluster_sync_all();                  // every rank's partial tile is in place
         if (warp >= 2) {
-            // This rank folds rows [lo, hi) (even bounds keep gate/up pairs together)
-            // for all tokens: P_0 + P_1 + ... in rank order, read through DSMEM.
+            // This rank folds rows [lo, hi) (multiples of 4) for all tokens: P_0 + P_1 + ...
+            // in rank order, four rows per thread, read through DSMEM.
             const int etid = threadIdx.x - 64;
-            const int lo = (split * (kTileRows / 2) / a.nsplit) * 2;
-            const int hi = ((split + 1) * (kTileRows / 2) / a.nsplit) * 2;
-            const int w = hi - lo;
-            const int count = w * a.M;
+            const int lo = (split * (kTileRows / 4) / a.nsplit) * 4;
+            const int hi = ((split + 1) * (kTileRows / 4) / a.nsplit) * 4;
+            const int w4 = (hi - lo) / 4;
+            const int count = w4 * a.M;
             const uint32_t pbase = smem_u32(smem);
-            const bool live = !*abort_flag;
-            for (int base = 0; base < count; base += 128) {
-                const int e = base + etid;
-                const bool valid = e < count && live;
-                const int t = valid ? e / w : 0;
-                const int r = valid ? lo + (e - t * w) : lo;
-                float y = 0.0f;
-                if (valid) {
-                    const uint32_t off = static_cast<uint32_t>((t * kTileRows + r) * 4);
-                    y = ld_dsmem_f32(map_to_rank(pbase + off, 0));
-                    for (int s2 = 1; s2 < a.nsplit; ++s2) y = y + ld_dsmem_f32(map_to_rank(pbase + off, s2));
+            uint32_t peer[kMaxCluster];
+#pragma unroll
+            for (int r = 0; r < kMaxCluster; ++r) peer[r] = r < a.nsplit ? map_to_rank(pbase, r) : 0u;
+            if (!*abort_flag) {
+#pragma unroll 1
+                for (int base = 0; base < count; base += 2 * 128) {
+                    float4 acc[2];
+                    int tt[2], rr[2];
+                    bool vv[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int e = base + u * 128 + etid;
+                        vv[u] = e < count;
+                        tt[u] = vv[u] ? e / w4 : 0;
+                        rr[u] = lo + 4 * (vv[u] ? e - tt[u] * w4 : 0);
+                        const uint32_t off = static_cast<uint32_t>((tt[u] * kTileRows + rr[u]) * 4);
+                        acc[u] = vv[u] ? ld_dsmem_f32x4(peer[0] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll
+                    for (int s2 = 1; s2 < kMaxCluster; ++s2) {
+                        if (s2 >= a.nsplit) break;
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            if (!vv[u]) continue;
+                            const float4 v = ld_dsmem_f32x4(peer[s2] + static_cast<uint32_t>((tt[u] * kTileRows + rr[u]) * 4));
+                            acc[u].x = acc[u].x + v.x;
+                            acc[u].y = acc[u].y + v.y;
+                            acc[u].z = acc[u].z + v.z;
+                            acc[u].w = acc[u].w + v.w;
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+                        if (vv[u]) emit4<EPI>(a, tt[u], tile * kTileRows + rr[u], acc[u]);
                 }
-                const int n2 = tile * kTileRows + r;
-                emit<EPI>(a, t, n2, y, valid && n2 < a.N);
             }
         }
         cluster_sync_all();                  // no rank leaves while others still read its partials
