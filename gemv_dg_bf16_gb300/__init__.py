@@ -10,7 +10,7 @@ from ._binding import (  # noqa: F401
     DG_VAR_CC_BULK, DG_VAR_CC_WARP, DG_VAR_DEFAULT, DG_VAR_TC, DGError, ROWS_BUCKETS, Choice,
     dg_build_id, dg_device_status, dg_device_status_clear, dg_gate_up_silu, dg_gemv_bf16, dg_head_fp8_argmax,
     dg_head_fp8_argmax_noalloc,
-    dg_init, dg_moe_w1_silu, dg_moe_w2, dg_select, dg_selection_space, dg_status_str, dg_sweep,
+    dg_init, dg_launch_flags, dg_moe_w1_silu, dg_set_launch_flags, DG_LAUNCH_PDL, dg_moe_w2, dg_select, dg_selection_space, dg_status_str, dg_sweep,
     dg_table_check, dg_table_clear, dg_table_entries, dg_table_load, dg_workspace_bytes, lib,
     library_path, workspace,
 )

@@ -81,6 +81,10 @@ def lib():
     L.dg_workspace_bytes.restype = Z
     L.dg_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), P]
     L.dg_device_status_clear.argtypes = [P, P]
+    L.dg_set_launch_flags.argtypes = [ctypes.c_uint]
+    L.dg_set_launch_flags.restype = S
+    L.dg_launch_flags.argtypes = []
+    L.dg_launch_flags.restype = ctypes.c_uint
     L.dg_gemv_bf16.argtypes = [P, P, P, I, I, I, P, Z, P, P]
     L.dg_gate_up_silu.argtypes = [P, P, P, I, I, I, P, Z, P, P]
     L.dg_head_fp8_argmax.argtypes = [P, P, P, P, P, I, I, I, P, Z, P, P]
@@ -140,6 +144,17 @@ def _check_dev(*ts):
 
 def dg_init(device: int = 0):
     _ok(lib().dg_init(int(device)), "dg_init")
+
+
+DG_LAUNCH_PDL = 0x1
+
+
+def dg_set_launch_flags(flags: int):
+    _ok(lib().dg_set_launch_flags(int(flags)), "dg_set_launch_flags")
+
+
+def dg_launch_flags() -> int:
+    return int(lib().dg_launch_flags())
 
 
 def dg_workspace_bytes(op: int, M: int, N: int, K: int, topk: int = 0) -> int:

@@ -2,6 +2,7 @@
 //
 // Nothing here allocates device memory or synchronises the host with a stream
 // (dg_device_status excepted, which exists for tests and health checks).
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -9,6 +10,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "dg_cc_bulk.cuh"
 #include "dg_cc_dense.cuh"
 #include "dg_internal.h"
 #include "dg_moe.cuh"
@@ -46,6 +48,28 @@ const DeviceInfo* current_device(dg_status* err)
     }
     std::lock_guard<std::mutex> lk(g_mu);
     return &g_dev[dev];
+}
+
+namespace {
+std::atomic<int> g_launch_flags{DG_LAUNCH_PDL};
+}
+
+bool pdl_enabled() { return (g_launch_flags.load(std::memory_order_relaxed) & DG_LAUNCH_PDL) != 0; }
+
+cudaError_t launch_kernel(const void* fn, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                          void** args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 int occupancy(const void* fn, int threads, size_t smem)
@@ -207,6 +231,15 @@ dg_status dg_device_status(const void* ws, int32_t* host_out, dg_stream_t stream
     return DG_OK;
 }
 
+dg_status dg_set_launch_flags(unsigned flags)
+{
+    if (flags & ~static_cast<unsigned>(DG_LAUNCH_PDL)) return DG_ERR_INVALID_ARG;
+    g_launch_flags.store(static_cast<int>(flags));
+    return DG_OK;
+}
+
+unsigned dg_launch_flags(void) { return static_cast<unsigned>(g_launch_flags.load()); }
+
 dg_status dg_device_status_clear(void* ws, dg_stream_t stream)
 {
     if (!ws) return DG_ERR_INVALID_ARG;
@@ -232,10 +265,56 @@ dg_status resolve_choice(dg_op op, int M, int N, int K, const dg_choice* in, dg_
     return dg_select(op, M, N, K, out);
 }
 
+// Bulk-staged variant: one (or two) persistent CTAs per SM, a deep shared-memory ring.
+dg_status launch_bulk(dg_op op, const DeviceInfo* dev, const dg_choice& c, DenseArgs a, int M, size_t ws_bytes,
+                      cudaStream_t stream)
+{
+    const int esz = (op == DG_OP_HEAD_FP8_ARGMAX) ? 1 : 2;
+    const int rw = (op == DG_OP_GATE_UP_SILU) ? 2 : 1;
+    const int cps = c.params[2] > 0 ? c.params[2] : 1;
+    if (c.params[0] != 0 || c.params[1] < 0 || c.params[1] > 32 || c.params[1] == 1 || cps > 2)
+        return DG_ERR_BAD_VARIANT;
+    int mt_max = static_cast<int>(kXsBudget / (static_cast<size_t>(a.K) * 2));
+    if (mt_max > 8) mt_max = 8;
+    if (mt_max < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+    if (op == DG_OP_HEAD_FP8_ARGMAX && M > mt_max) return DG_ERR_UNSUPPORTED_SHAPE;
+    const size_t stage = static_cast<size_t>(kBulkConsumers) * rw * kSeg * esz;
+    const size_t budget = (cps == 1 ? kMaxDynSmem : kMaxDynSmem / 2 - 8 * 1024);
+    for (int t0 = 0; t0 < M; t0 += mt_max) {
+        const int mt = (M - t0 < mt_max) ? M - t0 : mt_max;
+        const void* fn = op == DG_OP_GEMV_BF16      ? bulk_kernel_gemv(mt)
+                         : op == DG_OP_GATE_UP_SILU ? bulk_kernel_gateup(mt)
+                                                    : bulk_kernel_head(mt);
+        if (!fn) return DG_ERR_BAD_VARIANT;
+        const size_t xbytes = (static_cast<size_t>(mt) * a.K * 2 + 127) / 128 * 128;
+        if (xbytes + 2 * stage + 64 > budget) return DG_ERR_UNSUPPORTED_SHAPE;
+        int stages = c.params[1];
+        const int fit = static_cast<int>((budget - xbytes - 64) / (stage + 16));
+        if (stages == 0) stages = fit < 32 ? fit : 32;
+        if (stages < 2 || stages > fit) return DG_ERR_BAD_VARIANT;
+        const size_t smem = xbytes + static_cast<size_t>(stages) * (stage + 16);
+        const int occ = occupancy(fn, kBulkThreads, smem);
+        if (occ < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+        const long long grid = static_cast<long long>(dev->sm_count) * (occ < cps ? occ : cps);
+        if (op == DG_OP_HEAD_FP8_ARGMAX && ws_bytes < kWsData + static_cast<size_t>(grid) * cpow2(mt) * 8)
+            return DG_ERR_WORKSPACE_TOO_SMALL;
+        DenseArgs la = a;
+        la.t0 = t0;
+        void* args[] = {&la, &stages};
+        if (launch_kernel(fn, static_cast<unsigned>(grid), kBulkThreads, smem, stream, args) !=
+            cudaSuccess) {
+            cudaGetLastError();
+            return DG_ERR_CUDA;
+        }
+    }
+    return DG_OK;
+}
+
 // Launch the dense CUDA-core family over token chunks.
 dg_status launch_dense(dg_op op, const DeviceInfo* dev, const dg_choice& c, DenseArgs a, int M,
                        size_t ws_bytes, cudaStream_t stream)
 {
+    if (c.variant == DG_VAR_CC_BULK) return launch_bulk(op, dev, c, a, M, ws_bytes, stream);
     const int esz = (op == DG_OP_HEAD_FP8_ARGMAX) ? 1 : 2;
     (void)esz;
     int R = c.params[0] > 0 ? c.params[0] : 4;
@@ -273,7 +352,7 @@ dg_status launch_dense(dg_op op, const DeviceInfo* dev, const dg_choice& c, Dens
             ws_bytes < kWsData + static_cast<size_t>(grid) * cpow2(mt) * 8)
             return DG_ERR_WORKSPACE_TOO_SMALL;
         void* args[] = {&la};
-        if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads), args, smem, stream) !=
+        if (launch_kernel(fn, static_cast<unsigned>(grid), threads, smem, stream, args) !=
             cudaSuccess) {
             cudaGetLastError();
             return DG_ERR_CUDA;
@@ -313,7 +392,7 @@ dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int 
     if ((s = resolve_choice(DG_OP_GEMV_BF16, M, N, K, choice, &c)) != DG_OK) return s;
     if (c.variant == DG_VAR_TC)
         return launch_tc(false, dev, c, x, W, y, M, N, K, N, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
-    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    if (c.variant != DG_VAR_CC_WARP && c.variant != DG_VAR_CC_BULK) return DG_ERR_BAD_VARIANT;
     DenseArgs a{};
     a.W = static_cast<const uint8_t*>(W);
     a.x = static_cast<const uint16_t*>(x);
@@ -341,7 +420,7 @@ dg_status dg_gate_up_silu(const void* x, const void* W_gu, void* out, int M, int
     if (c.variant == DG_VAR_TC)
         return launch_tc(true, dev, c, x, W_gu, out, M, 2 * N_half, K, N_half, ws, ws_bytes,
                          reinterpret_cast<cudaStream_t>(stream));
-    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    if (c.variant != DG_VAR_CC_WARP && c.variant != DG_VAR_CC_BULK) return DG_ERR_BAD_VARIANT;
     DenseArgs a{};
     a.W = static_cast<const uint8_t*>(W_gu);
     a.x = static_cast<const uint16_t*>(x);
@@ -369,7 +448,7 @@ dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, 
     if (!dev) return s;
     dg_choice c;
     if ((s = resolve_choice(DG_OP_HEAD_FP8_ARGMAX, M, N, K, choice, &c)) != DG_OK) return s;
-    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    if (c.variant != DG_VAR_CC_WARP && c.variant != DG_VAR_CC_BULK) return DG_ERR_BAD_VARIANT;
     DenseArgs a{};
     a.W = static_cast<const uint8_t*>(Wq);
     a.x = static_cast<const uint16_t*>(x);
@@ -403,7 +482,7 @@ static dg_status launch_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, 
     if (c.params[2] > 0 && occ > c.params[2]) occ = c.params[2];
     const long long grid = static_cast<long long>(dev->sm_count) * occ;
     void* args[] = {&a};
-    if (cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(threads), args, smem, stream) !=
+    if (launch_kernel(fn, static_cast<unsigned>(grid), threads, smem, stream, args) !=
         cudaSuccess) {
         cudaGetLastError();
         return DG_ERR_CUDA;

@@ -167,6 +167,18 @@ __global__ void __launch_bounds__(256) cc_dense_kernel(DenseArgs a)
     const int wpc = blockDim.x >> 5;
     const int kv = a.K / 8;
 
+    // Weights only: start the first segment of this warp's first row group on its way
+    // into L2 while a preceding kernel may still be finishing, then wait for it.
+    {
+        const int g0 = blockIdx.x * wpc + warp;
+        const int row = g0 * R + lane;
+        if (lane < R && g0 < a.groups && row < a.N)
+            prefetch_l2(a.W + static_cast<size_t>(row) * a.K * WTraits<WT>::ESZ,
+                        static_cast<uint32_t>(min(a.K, kSeg) * WTraits<WT>::ESZ));
+    }
+    pdl_launch_dependents();
+    pdl_wait();
+
     // Stage this chunk's activations.
     for (int i = threadIdx.x; i < MT * kv; i += blockDim.x) {
         const int t = i / kv, c = i - t * kv;

@@ -217,6 +217,8 @@ __global__ void __launch_bounds__(256) moe_kernel(MoeArgs a)
     __shared__ Route R;
     __shared__ int fold_flag;
     extern __shared__ uint4 xs[];        // [kMoeMT][K/8]
+    pdl_launch_dependents();
+    pdl_wait();                          // routing and activations come from earlier kernels
     route_scan(R, a.ids, a.M, a.topk, a.E, a.ws);
 
     const int rows = W1 ? a.I : a.Nout;                 // N-tiles cut these rows (W1: columns j)

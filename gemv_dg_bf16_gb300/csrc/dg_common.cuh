@@ -19,6 +19,8 @@
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
 
+#include "dg.h"
+
 namespace dg {
 
 constexpr int kSeg = 1024;                 // K elements per canonical segment
@@ -127,6 +129,20 @@ __device__ __forceinline__ void reduce_scatter(float (&v)[Q], int lane)
 {
     static_assert(Q >= 1 && Q <= 32 && (Q & (Q - 1)) == 0, "Q must be a power of two <= 32");
     Butterfly<16, Q>::run(v, lane);
+}
+
+// Programmatic dependent launch.  A kernel may read weights (never written by this
+// library's kernels) before pdl_wait(); everything a preceding kernel may have
+// produced or may still read (activations, routing, scales, outputs, workspace) is
+// touched only after it.  pdl_wait() returns at once when the launch had no
+// programmatic dependency.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// Pull `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Greedy-pick order: larger value first, then lower index; NaN never wins.

@@ -4,4 +4,5 @@
 
 namespace dg {
 const void* dense_kernel_gemv(int mt, int R) { return dense_lookup<WT_BF16, EPI_STORE>(mt, R); }
+const void* bulk_kernel_gemv(int mt) { return bulk_lookup<WT_BF16, EPI_STORE>(mt); }
 }  // namespace dg

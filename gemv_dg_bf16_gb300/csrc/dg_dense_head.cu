@@ -4,4 +4,5 @@
 
 namespace dg {
 const void* dense_kernel_head(int mt, int R) { return dense_lookup<WT_E4M3, EPI_HEAD>(mt, R); }
+const void* bulk_kernel_head(int mt) { return bulk_lookup<WT_E4M3, EPI_HEAD>(mt); }
 }  // namespace dg

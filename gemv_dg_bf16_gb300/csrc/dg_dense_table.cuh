@@ -3,6 +3,7 @@
 // one warp reduction (and, for gate/up, even R) are built.
 #pragma once
 
+#include "dg_cc_bulk.cuh"
 #include "dg_cc_dense.cuh"
 
 namespace dg {
@@ -46,6 +47,30 @@ const void* dense_lookup(int mt, int R)
     case 6: return dense_by_r<WT, EPI, 6>(R);
     case 7: return dense_by_r<WT, EPI, 7>(R);
     case 8: return dense_by_r<WT, EPI, 8>(R);
+    default: return nullptr;
+    }
+}
+
+// Bulk-staged variant: RW rows per consumer warp (a (gate, up) pair for gate/up).
+template <int WT, int EPI, int MT>
+const void* bulk_one()
+{
+    constexpr int RW = EPI == EPI_GATEUP ? 2 : 1;
+    return reinterpret_cast<const void*>(&cc_bulk_kernel<WT, MT, RW, EPI>);
+}
+
+template <int WT, int EPI>
+const void* bulk_lookup(int mt)
+{
+    switch (mt) {
+    case 1: return bulk_one<WT, EPI, 1>();
+    case 2: return bulk_one<WT, EPI, 2>();
+    case 3: return bulk_one<WT, EPI, 3>();
+    case 4: return bulk_one<WT, EPI, 4>();
+    case 5: return bulk_one<WT, EPI, 5>();
+    case 6: return bulk_one<WT, EPI, 6>();
+    case 7: return bulk_one<WT, EPI, 7>();
+    case 8: return bulk_one<WT, EPI, 8>();
     default: return nullptr;
     }
 }

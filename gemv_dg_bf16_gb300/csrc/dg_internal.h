@@ -14,6 +14,10 @@ namespace dg {
 const void* dense_kernel_gemv(int mt, int R);
 const void* dense_kernel_gateup(int mt, int R);
 const void* dense_kernel_head(int mt, int R);
+// Bulk-staged variant of the same family (dg_cc_bulk.cuh), by tokens in the chunk.
+const void* bulk_kernel_gemv(int mt);
+const void* bulk_kernel_gateup(int mt);
+const void* bulk_kernel_head(int mt);
 
 // MoE kernels (rows per warp fixed per family; tokens per chunk chosen on device).
 const void* moe_w1_kernel();
@@ -44,6 +48,11 @@ const DeviceInfo* current_device(dg_status* err);
 // Resident CTAs per SM for `fn` with `threads` threads and `smem` dynamic bytes
 // (cached); also raises the kernel's dynamic shared memory limit once.
 int occupancy(const void* fn, int threads, size_t smem);
+
+// Launch with this library's attributes (programmatic dependent launch when enabled).
+bool pdl_enabled();
+cudaError_t launch_kernel(const void* fn, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
+                          void** args);
 
 // Maximum dynamic shared memory any launch of this library asks for.
 constexpr size_t kMaxDynSmem = 200 * 1024;

@@ -191,6 +191,14 @@ std::string check_choice(int op, const dg_choice& c)
             if (c.params[i] != 0) return "unused tensor-core parameter set";
         return "";
     }
+    if (c.variant == DG_VAR_CC_BULK) {
+        if (op != DG_OP_GEMV_BF16 && op != DG_OP_GATE_UP_SILU && op != DG_OP_HEAD_FP8_ARGMAX)
+            return "no bulk-staged variant for this op";
+        if (c.params[0] != 0 || c.params[1] < 0 || c.params[1] == 1 || c.params[1] > 32 || c.params[2] < 0 ||
+            c.params[2] > 2)
+            return "bulk-staged parameters out of range";
+        return "";
+    }
     if (c.variant != DG_VAR_CC_WARP) return "variant not in this build's selection space";
     const int R = c.params[0], wpc = c.params[1];
     if (op == DG_OP_MOE_W1 || op == DG_OP_MOE_W2) {
@@ -365,7 +373,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 2; }
+int dg_selection_space(void) { return 3; }
 
 const char* dg_build_id(void) { return build_id(); }
 

@@ -95,7 +95,8 @@ dg_choice mk(int v, int p0, int p1 = 0, int p2 = 0, int p3 = 0)
     return c;
 }
 
-// Candidates of the default's family (families never mix inside a bucket).
+// Candidates of the default's family (families never mix inside a bucket; the
+// register-streamed and bulk-staged CUDA-core variants are one family).
 std::vector<dg_choice> candidates(int op, const dg_choice& def)
 {
     std::vector<dg_choice> out{def};
@@ -118,6 +119,8 @@ std::vector<dg_choice> candidates(int op, const dg_choice& def)
                 if (op == DG_OP_GATE_UP_SILU && R < 2) continue;
                 add(mk(DG_VAR_CC_WARP, R, wpc, 0));
             }
+        for (int cps : {1, 2})
+            for (int st : {0, 4, 8}) add(mk(DG_VAR_CC_BULK, 0, st, cps));
     }
     return out;
 }

@@ -274,9 +274,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), accum = smem_u32(bars + 2 * S);
 
+    pdl_launch_dependents();
     if (warp == 0) {
         if (lane == 0) {
-            for (int i = 0; i < nkb; ++i) {
+            // Weight boxes of the first ring fill do not depend on earlier kernels:
+            // issue them before waiting, the activation boxes after.
+            const int pre = nkb < S ? nkb : S;
+            for (int i = 0; i < pre; ++i) {
+                const uint32_t dst = smem_u32(smem + i * kStage);
+                mbar_expect_tx(full0 + 8 * i, kStage);
+                tma_load_2d(dst, &tmW, (kb0 + i) * kKB, tile * kTileRows, full0 + 8 * i);
+            }
+            pdl_wait();
+            for (int i = 0; i < pre; ++i)
+                tma_load_2d(smem_u32(smem + i * kStage) + kWBox, &tmX, (kb0 + i) * kKB, 0, full0 + 8 * i);
+            for (int i = pre; i < nkb; ++i) {
                 const int s = i % S;
                 const uint32_t round = static_cast<uint32_t>(i / S);
                 if (!mbar_wait(empty0 + 8 * s, (round & 1u) ^ 1u, abort_flag)) break;
@@ -286,8 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(dst, &tmW, k, tile * kTileRows, full0 + 8 * s);
                 tma_load_2d(dst + kWBox, &tmX, k, 0, full0 + 8 * s);
             }
+        } else {
+            pdl_wait();
         }
     } else if (warp == 1) {
+        pdl_wait();
         if (lane == 0) {
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % S;
@@ -304,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(accum);           // fires once every MMA issued above has completed
         }
     } else {
+        pdl_wait();
         // Epilogue warps 2..5 -> TMEM lane quarter (warp % 4).
         const int q = warp & 3;
         const int row = q * 32 + lane;
@@ -512,13 +528,15 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(a.nsplit);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
         cudaGetLastError();
         return DG_ERR_CUDA;

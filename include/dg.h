@@ -83,7 +83,7 @@ typedef enum {
 /* params[] meaning by variant:
  *   DG_VAR_CC_WARP: [0] rows per warp R (1, 2, 4, 8), [1] warps per CTA (2..16),
  *                   [2] CTAs per SM cap (0 = occupancy limit)
- *   DG_VAR_CC_BULK: [0] rows per stage, [1] pipeline stages, [2] consumer warps
+ *   DG_VAR_CC_BULK: [0] 0, [1] pipeline stages (0 = as many as fit), [2] CTAs per SM (0 = 1)
  *   DG_VAR_TC:      [0] pipeline stages, [1] K-splits (0 = derived from the shape)
  * For the MoE ops, params[3] is the N-tile width in rows (0 = derived). */
 typedef struct {
@@ -121,6 +121,20 @@ size_t dg_workspace_bytes(dg_op op, int M, int N, int K, int topk);
 /* Copy the workspace's device status word to *host_out (synchronises `stream`;
  * meant for tests and health checks, not the decode loop). */
 dg_status dg_device_status(const void* ws, int32_t* host_out, dg_stream_t stream);
+
+/* Launch flags (process-wide).  DG_LAUNCH_PDL (on by default): every kernel is
+ * launched with programmatic dependent launch, so it can be scheduled while the
+ * preceding kernel on the stream finishes; before waiting for that kernel it
+ * touches nothing but weights (streams them into L2 or shared memory), which this
+ * library never writes.  A preceding kernel that does not signal early (any
+ * kernel not from this library) still completes before this one starts its
+ * dependent work.  Turn it off when a kernel of this library must wait for a
+ * preceding launch that writes the weights it reads.
+ * "Decode optimization round 3", "Profiling" / "Remaining headroom": decode steps
+ * are bound by per-kernel launch latency, not bandwidth. */
+#define DG_LAUNCH_PDL 0x1u
+dg_status dg_set_launch_flags(unsigned flags);
+unsigned dg_launch_flags(void);
 
 /* Clear the device status word (asynchronous on `stream`). */
 dg_status dg_device_status_clear(void* ws, dg_stream_t stream);
