@@ -104,20 +104,32 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
             break;
         }
         // Enough 8-warp CTAs to put two on every SM of a 152-SM part.
+        // Rows per warp / warps per CTA as measured on GB300 (dg_sweep): one row per
+        // warp at M = 1, more rows per warp as M grows (x reuse), small CTAs.
         const long rows = op == DG_OP_GATE_UP_SILU ? 2L * N : static_cast<long>(N);
-        out->params[0] = rows >= 304L * 32 ? 4 : (rows >= 304L * 16 ? 2 : (op == DG_OP_GATE_UP_SILU ? 2 : 1));
-        out->params[1] = 8;
+        if (M <= 1)
+            out->params[0] = op == DG_OP_GATE_UP_SILU ? 2 : (rows >= 8192 && rows < 16384 ? 2 : 1);
+        else if (M <= 2)
+            out->params[0] = rows >= 8192 ? 4 : 2;
+        else
+            out->params[0] = rows >= 8192 ? 4 : 2;
+        out->params[1] = 4;
         break;
     }
     case DG_OP_HEAD_FP8_ARGMAX:
-        out->params[0] = M <= 2 ? 8 : (M <= 4 ? 4 : 4);
-        out->params[1] = 8;
+        // measured on GB300 (dg_sweep over the 248320 x 4096 head)
+        out->params[0] = M == 4 ? 4 : (M <= 3 ? 8 : 4);
+        out->params[1] = M <= 4 ? 4 : 8;
         break;
     case DG_OP_MOE_W1:
-    case DG_OP_MOE_W2:
         out->params[0] = 4;
         out->params[1] = 8;
-        out->params[3] = 0;
+        out->params[3] = M <= 1 ? 32 : 64;   // gate/up columns per work unit
+        break;
+    case DG_OP_MOE_W2:
+        out->params[0] = 4;
+        out->params[1] = 4;
+        out->params[3] = M <= 8 ? 64 : 128;  // output rows per work unit
         break;
     default:
         break;

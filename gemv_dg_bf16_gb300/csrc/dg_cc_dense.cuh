@@ -52,29 +52,19 @@ __device__ __forceinline__ void fma_vector(const uint4 (&w)[R], const uint4* xs,
                                            float (&p)[R * MTP])
 {
     if constexpr (WT == WT_BF16) {
+        // bf16 x bf16 products are exact in fp32, so the mixed-precision fma (bf16
+        // operands, fp32 addend, one rounding) gives the same bits as converting
+        // both operands to fp32 first -- without the conversions.
         uint4 xv[MT];
 #pragma unroll
         for (int t = 0; t < MT; ++t) xv[t] = xs[t * xstride];
 #pragma unroll
         for (int wd = 0; wd < 4; ++wd) {
-            float x0[MT], x1[MT];
-#pragma unroll
-            for (int t = 0; t < MT; ++t) {
-                const uint32_t xw = (&xv[t].x)[wd];
-                x0[t] = bf16_lo(xw);
-                x1[t] = bf16_hi(xw);
-            }
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint32_t ww = (&w[r].x)[wd];
-                const float w0 = bf16_lo(ww), w1 = bf16_hi(ww);
 #pragma unroll
-                for (int t = 0; t < MT; ++t) {
-                    float acc = p[r * MTP + t];
-                    acc = __fmaf_rn(x0[t], w0, acc);
-                    acc = __fmaf_rn(x1[t], w1, acc);
-                    p[r * MTP + t] = acc;
-                }
+                for (int t = 0; t < MT; ++t) fma2_bf16(p[r * MTP + t], (&xv[t].x)[wd], ww);
             }
         }
     } else {
@@ -113,41 +103,63 @@ __device__ __forceinline__ void fma_vector(const uint4 (&w)[R], const uint4* xs,
     }
 }
 
+// Load this lane's VPS vectors of segment s for R rows (zero outside the matrix).
+template <int WT, int R>
+__device__ __forceinline__ void load_segment(uint4 (&w)[kSeg / (32 * WTraits<WT>::VE)][R],
+                                             const uint8_t* const (&wrow)[R], const bool (&rok)[R], int K,
+                                             int s, int lane)
+{
+    using T = WTraits<WT>;
+    constexpr int VE = T::VE;
+    constexpr int VPS = kSeg / (32 * VE);
+#pragma unroll
+    for (int v = 0; v < VPS; ++v) {
+        const int k = s * kSeg + v * (32 * VE) + lane * VE;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            w[v][r] = (rok[r] && k < K) ? ld_stream(wrow[r] + static_cast<size_t>(k) * T::ESZ)
+                                        : make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Canonical-order partial of segment s (lane chains, then the butterfly), folded
+// into `total`.
+template <int WT, int MT, int R>
+__device__ __forceinline__ void fold_segment(const uint4 (&w)[kSeg / (32 * WTraits<WT>::VE)][R], int K, int s,
+                                             const uint4* xs_smem, int xstride, int lane, float& total)
+{
+    constexpr int VE = WTraits<WT>::VE;
+    constexpr int VPS = kSeg / (32 * VE);
+    constexpr int MTP = cpow2(MT);
+    constexpr int Q = R * MTP;
+    float p[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) p[q] = 0.0f;
+#pragma unroll
+    for (int v = 0; v < VPS; ++v) {
+        const int k = s * kSeg + v * (32 * VE) + lane * VE;
+        if (k < K) fma_vector<WT, MT, R, MTP>(w[v], xs_smem + k / 8, xstride, p);
+    }
+    reduce_scatter<Q>(p, lane);
+    total = (s == 0) ? p[0] : total + p[0];
+}
+
 // One row group: returns this lane's folded total for output index
-// idx = lane >> SH, i.e. (r = idx / MTP, t = idx % MTP).
+// idx = lane >> SH, i.e. (r = idx / MTP, t = idx % MTP).  (Loading segment s + 1
+// before reducing segment s was measured on GB300: it costs occupancy and loses
+// more than it hides, most of all for e4m3 rows.)
 template <int WT, int MT, int R>
 __device__ __forceinline__ float row_group_total(const uint8_t* const (&wrow)[R],
                                                  const bool (&rok)[R], int K,
                                                  const uint4* xs_smem, int xstride, int lane)
 {
-    using T = WTraits<WT>;
-    constexpr int VE = T::VE;
-    constexpr int VPS = kSeg / (32 * VE);
-    constexpr int MTP = cpow2(MT);
-    constexpr int Q = R * MTP;
+    constexpr int VPS = kSeg / (32 * WTraits<WT>::VE);
     const int nseg = (K + kSeg - 1) / kSeg;
-
     float total = 0.0f;
     for (int s = 0; s < nseg; ++s) {
         uint4 w[VPS][R];
-#pragma unroll
-        for (int v = 0; v < VPS; ++v) {
-            const int k = s * kSeg + v * (32 * VE) + lane * VE;
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-                w[v][r] = (rok[r] && k < K) ? ld_stream(wrow[r] + static_cast<size_t>(k) * T::ESZ)
-                                             : make_uint4(0, 0, 0, 0);
-        }
-        float p[Q];
-#pragma unroll
-        for (int q = 0; q < Q; ++q) p[q] = 0.0f;
-#pragma unroll
-        for (int v = 0; v < VPS; ++v) {
-            const int k = s * kSeg + v * (32 * VE) + lane * VE;
-            if (k < K) fma_vector<WT, MT, R, MTP>(w[v], xs_smem + k / 8, xstride, p);
-        }
-        reduce_scatter<Q>(p, lane);
-        total = (s == 0) ? p[0] : total + p[0];
+        load_segment<WT, R>(w, wrow, rok, K, s, lane);
+        fold_segment<WT, MT, R>(w, K, s, xs_smem, xstride, lane, total);
     }
     return total;
 }

@@ -76,6 +76,19 @@ __device__ __forceinline__ int ld_cg_s32(const int* p)
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// acc = fma(x.lo, w.lo, acc); acc = fma(x.hi, w.hi, acc) on packed bf16 pairs, with
+// the mixed-precision fma (bf16 operands, fp32 addend and result, one rounding).
+__device__ __forceinline__ void fma2_bf16(float& acc, uint32_t x2, uint32_t w2)
+{
+    asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\t"
+        "mov.b32 {xl, xh}, %1;\n\t"
+        "mov.b32 {wl, wh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, xl, wl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, xh, wh, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(x2), "r"(w2));
+}
+
 // Two e4m3 codes (low byte = first element) -> two fp32 values (exact), via the
 // hardware e4m3x2 -> f16x2 conversion followed by f16 -> f32.
 __device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two_codes)
