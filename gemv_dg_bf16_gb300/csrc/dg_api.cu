@@ -93,7 +93,6 @@ int occupancy(const void* fn, int threads, size_t smem)
 
 void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
 {
-    (void)K;
     std::memset(out, 0, sizeof *out);
     out->variant = DG_VAR_CC_WARP;
     switch (op) {
@@ -117,6 +116,10 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
         break;
     }
     case DG_OP_HEAD_FP8_ARGMAX:
+        if (M >= kTcHeadMinRows && K <= kTcHeadMaxK) {
+            out->variant = DG_VAR_TC;      // fp8 MMA on split activations
+            break;
+        }
         // measured on GB300 (dg_sweep over the 248320 x 4096 head)
         out->params[0] = M == 4 ? 4 : (M <= 3 ? 8 : 4);
         out->params[1] = M <= 4 ? 4 : 8;
@@ -460,6 +463,9 @@ dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, 
     if (!dev) return s;
     dg_choice c;
     if ((s = resolve_choice(DG_OP_HEAD_FP8_ARGMAX, M, N, K, choice, &c)) != DG_OK) return s;
+    if (c.variant == DG_VAR_TC)
+        return launch_tc_head(dev, c, x, Wq, scale, logits, argmax, M, N, K, ws, ws_bytes,
+                              reinterpret_cast<cudaStream_t>(stream));
     if (c.variant != DG_VAR_CC_WARP && c.variant != DG_VAR_CC_BULK) return DG_ERR_BAD_VARIANT;
     DenseArgs a{};
     a.W = static_cast<const uint8_t*>(Wq);

@@ -33,6 +33,16 @@ struct DeviceInfo;
 dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W,
                     void* out, int M, int N, int K, int ld_out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+// tcgen05 fp8 head (dg_tc_head.cu): shared memory for (K, stages) and the launcher.
+size_t tc_head_smem(int K, int stages);
+dg_status launch_tc_head(const DeviceInfo* dev, const dg_choice& c, const void* x, const void* Wq,
+                         const float* scale, void* logits, int32_t* argmax, int M, int N, int K, void* ws,
+                         size_t ws_bytes, cudaStream_t stream);
+// Smallest row bucket the fp8 head sends to the tensor cores, and the largest K
+// whose split activations fit in shared memory.
+constexpr int kTcHeadMinRows = 2;
+constexpr int kTcHeadMaxK = 8192;
+
 struct DeviceInfo {
     int device = -1;
     int sm_count = 0;

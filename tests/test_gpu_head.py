@@ -38,12 +38,16 @@ def _check_argmax(x, Wq, scale, am):
         assert gap[m] <= window and lg[0, 0] - lg[0, 1] <= window, (m, got[m], idx[m], gap[m])
 
 
-@pytest.mark.parametrize("bulk", [False, True])
+FAMILIES = {"default": None, "cc": dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0),
+            "bulk": dg.Choice.make(dg.DG_VAR_CC_BULK, 0, 0, 0), "tc": dg.Choice.make(dg.DG_VAR_TC, 0)}
+
+
+@pytest.mark.parametrize("family", ["default", "cc", "bulk", "tc"])
 @pytest.mark.parametrize("M,N,K", [(1, 1000, 4096), (2, 777, 1040), (3, 4099, 512), (5, 300, 2064),
-                                   (8, 2048, 4096), (4, 1, 16)])
-def test_head_small_exhaustive(cuda_device, M, N, K, bulk):
+                                   (8, 2048, 4096), (4, 1, 16), (6, 130, 4096)])
+def test_head_small_exhaustive(cuda_device, M, N, K, family):
     x, Wq, scale = S.head_inputs(M, N, K, device=cuda_device)
-    c = dg.Choice.make(dg.DG_VAR_CC_BULK, 0, 0, 0) if bulk else None
+    c = FAMILIES[family]
     logits, am = dg.dg_head_fp8_argmax(x, Wq, scale, choice=c)
     torch.cuda.synchronize()
     _check_logits(x, Wq, scale, logits)
@@ -69,9 +73,34 @@ def test_head_full_size(cuda_device, full_head, M):
     assert torch.equal(am, am2)
 
 
+def test_head_tc_variants_bitwise_identical(cuda_device):
+    x, Wq, scale = S.head_inputs(6, 20000, 4096, device=cuda_device)
+    ref_l, ref_a = dg.dg_head_fp8_argmax(x, Wq, scale, choice=FAMILIES["tc"])
+    for st in (2, 3, 5, 8):
+        l, a = dg.dg_head_fp8_argmax(x, Wq, scale, choice=dg.Choice.make(dg.DG_VAR_TC, st))
+        assert torch.equal(l.view(torch.int16), ref_l.view(torch.int16)), st
+        assert torch.equal(a, ref_a), st
+    for _ in range(3):
+        l, a = dg.dg_head_fp8_argmax(x, Wq, scale, choice=FAMILIES["tc"])
+        assert torch.equal(l.view(torch.int16), ref_l.view(torch.int16)) and torch.equal(a, ref_a)
+
+
+def test_head_tc_activations_with_wide_dynamic_range(cuda_device):
+    """The hi/lo e4m3 split of the activations: tiny and large entries in one row."""
+    M, N, K = 3, 3000, 2048
+    x, Wq, scale = S.head_inputs(M, N, K, device=cuda_device)
+    g = torch.Generator().manual_seed(9)
+    mag = torch.exp2(torch.randint(-30, 12, (M, K), generator=g).float())
+    x = (torch.randn((M, K), generator=g) * mag).to(torch.bfloat16).to(cuda_device)
+    logits, am = dg.dg_head_fp8_argmax(x, Wq, scale, choice=FAMILIES["tc"])
+    torch.cuda.synchronize()
+    _check_logits(x, Wq, scale, logits)
+    _check_argmax(x, Wq, scale, am)
+
+
 def test_head_variants_bitwise_identical(cuda_device):
     x, Wq, scale = S.head_inputs(5, 3001, 2064, device=cuda_device)
-    ref_l, ref_a = dg.dg_head_fp8_argmax(x, Wq, scale)
+    ref_l, ref_a = dg.dg_head_fp8_argmax(x, Wq, scale, choice=FAMILIES["cc"])
     choices = [dg.Choice.make(dg.DG_VAR_CC_WARP, R, wpc, cap)
                for R in (1, 2, 4, 8) for wpc in (2, 4, 8) for cap in (0, 1)]
     choices += [dg.Choice.make(dg.DG_VAR_CC_BULK, 0, st, cps) for st in (0, 2, 5, 16) for cps in (1, 2)]
@@ -85,10 +114,10 @@ def test_head_variants_bitwise_identical(cuda_device):
         assert torch.equal(a, ref_a), repr(c)
 
 
-@pytest.mark.parametrize("bulk", [False, True])
-def test_head_ties_go_to_lowest_index(cuda_device, bulk):
+@pytest.mark.parametrize("family", ["cc", "bulk", "tc"])
+def test_head_ties_go_to_lowest_index(cuda_device, family):
     M, N, K = 3, 5000, 1024
-    c = dg.Choice.make(dg.DG_VAR_CC_BULK, 0, 0, 0) if bulk else None
+    c = FAMILIES[family]
     x, Wq, scale = S.head_inputs(M, N, K, device=cuda_device)
     _, am = dg.dg_head_fp8_argmax(x, Wq, scale, choice=c)
     for m in range(M):
@@ -103,18 +132,20 @@ def test_head_ties_go_to_lowest_index(cuda_device, bulk):
     assert a0.tolist() == [0] * M and (l0.float() == 0).all()
 
 
-def test_head_nan_rows_never_win(cuda_device):
+@pytest.mark.parametrize("family", ["cc", "tc"])
+def test_head_nan_rows_never_win(cuda_device, family):
     M, N, K = 2, 600, 512
+    c = FAMILIES[family]
     x, Wq, scale = S.head_inputs(M, N, K, device=cuda_device)
-    _, am = dg.dg_head_fp8_argmax(x, Wq, scale)
+    _, am = dg.dg_head_fp8_argmax(x, Wq, scale, choice=c)
     W2 = Wq.clone()
     for m in range(M):
         W2[int(am[m]), 7] = 0x7F             # e4m3 NaN code
-    _, am2 = dg.dg_head_fp8_argmax(x, W2, scale)
+    _, am2 = dg.dg_head_fp8_argmax(x, W2, scale, choice=c)
     idx, _, _ = O.head_argmax(bits16(x), W2.cpu().numpy(), float(scale.cpu()[0]))
     assert am2.cpu().numpy().tolist() == idx.tolist()
     allnan = torch.full_like(Wq, 0x7F)
-    _, a3 = dg.dg_head_fp8_argmax(x, allnan, scale)
+    _, a3 = dg.dg_head_fp8_argmax(x, allnan, scale, choice=c)
     assert a3.tolist() == [-1] * M
 
 
