@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -162,8 +163,17 @@ def run_gpu(args):
 
     cases = []        # (name, dict(meta), graph, weight_bytes_per_call)
     keep = []         # every tensor a captured graph reads or writes stays alive with it
+    pattern = re.compile(args.cases) if args.cases else None
+
+    def case_id(name, meta):
+        return name + "/" + "/".join(f"{k}{v}" for k, v in meta.items() if k in ("M", "N", "K", "N_half"))
+
+    def wanted(name, meta):
+        return pattern is None or pattern.search(case_id(name, meta)) is not None
 
     def add(name, meta, calls, wbytes):
+        if not wanted(name, meta):
+            return
         with torch.cuda.stream(stream):
             g = _graph_case(torch, calls, R, stream)
         cases.append((name, meta, g, wbytes))
@@ -175,6 +185,8 @@ def run_gpu(args):
     if args.only:
         only = tuple(int(v) for v in args.only.split(","))       # M,N,K
     for (N, K) in SWEEP_NK if only is None else [(only[1], only[2])]:
+        if not any(wanted("gemv_bf16", {"M": M, "N": N, "K": K}) for M in SWEEP_M):
+            continue
         W0 = S.linear_inputs(1, N, K, device=dev)[1]
         wb = N * K * 2
         Ws = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)]
@@ -183,8 +195,12 @@ def run_gpu(args):
             y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
             ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K, device=dev)
             calls = [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Ws]
-            add("gemv_bf16", {"M": M, "N": N, "K": K}, calls, wb)
-            sweep_cases.append(len(cases) - 1)
+            if wanted("gemv_bf16", {"M": M, "N": N, "K": K}):
+                add("gemv_bf16", {"M": M, "N": N, "K": K}, calls, wb)
+                sweep_cases.append(len(cases) - 1)
+    def need(name, metas):
+        return any(wanted(name, m) for m in metas)
+
     if not args.sweep_only and only is None:
         # --- GEMV 2048x1024 at M=1
         N, K = 2048, 1024
@@ -197,18 +213,21 @@ def run_gpu(args):
             [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Ws], wb)
         # --- gate/up
         Nh, K = 12288, 4096
-        W0 = S.gate_up_inputs(1, Nh, K, device=dev)[1]
+        W0 = (S.gate_up_inputs(1, Nh, K, device=dev)[1]
+              if need("gate_up_silu", [{"M": M, "N_half": Nh, "K": K} for M in GATE_UP_M]) else None)
         wb = 2 * Nh * K * 2
-        Ws = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)]
-        for M in GATE_UP_M:
+        Ws = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)] if W0 is not None else []
+        for M in GATE_UP_M if Ws else []:
             x = S.gate_up_inputs(M, Nh, K, device=dev)[0]
             out = torch.empty((M, Nh), dtype=torch.bfloat16, device=dev)
             ws = dg.workspace(dg.DG_OP_GATE_UP_SILU, M, Nh, K, device=dev)
             add("gate_up_silu", {"M": M, "N_half": Nh, "K": K},
                 [(lambda W=W, x=x, out=out, ws=ws: dg.dg_gate_up_silu(x, W, out, ws=ws, stream=stream)) for W in Ws], wb)
         # --- fp8 head
-        x8, Wq, scale = S.head_inputs(8, HEAD_N, HEAD_K, device=dev)
-        for M in HEAD_M:
+        head_on = need("head_fp8_argmax", [{"M": M, "N": HEAD_N, "K": HEAD_K} for M in HEAD_M])
+        if head_on:
+            x8, Wq, scale = S.head_inputs(8, HEAD_N, HEAD_K, device=dev)
+        for M in HEAD_M if head_on else []:
             x = x8[:M].contiguous()
             logits = torch.empty((M, HEAD_N), dtype=torch.bfloat16, device=dev)
             am = torch.empty((M,), dtype=torch.int32, device=dev)
@@ -217,8 +236,10 @@ def run_gpu(args):
                 [lambda x=x, logits=logits, am=am, ws=ws, Wq=Wq, scale=scale: dg.dg_head_fp8_argmax(
                     x, Wq, scale, logits, am, ws=ws, stream=stream)], HEAD_N * HEAD_K + 4)
         # --- MoE
-        W1q, s1, W2q, s2 = S.moe_weights(MOE_E, MOE_I, MOE_K, MOE_K, device=dev)
-        for M in MOE_M:
+        moe_on = need("moe_w1_silu", [{"M": M} for M in MOE_M]) or need("moe_w2", [{"M": M} for M in MOE_M])
+        if moe_on:
+            W1q, s1, W2q, s2 = S.moe_weights(MOE_E, MOE_I, MOE_K, MOE_K, device=dev)
+        for M in MOE_M if moe_on else []:
             routs = [S.moe_inputs(M, MOE_K, MOE_TOPK, MOE_E, rep=r, device=dev) for r in range(8)]
             uniq = [len(set(r[1].cpu().flatten().tolist())) for r in routs]
             a = torch.empty((M, MOE_TOPK, MOE_I), dtype=torch.bfloat16, device=dev)
@@ -278,6 +299,8 @@ def run_gpu(args):
                     weight_bytes=int(wb))
 
     sweep = [summarize(i) for i in sweep_cases]
+    if not sweep:                       # profiling runs of other ops: report their totals
+        sweep = [summarize(i) for i in range(n_cases)]
     step_us = sum(s["us"] for s in sweep)
     step_bytes = sum(s["weight_bytes"] for s in sweep)
     value_rank = step_bytes / (step_us * 1e-6) / 1e9
@@ -295,7 +318,7 @@ def run_gpu(args):
         ops.setdefault(s["op"], []).append(s)
 
     # ---- e2e through the public API with host buffers (x in, y out, pinned)
-    e2e = _e2e(torch, dg, S, dev, stream, args, l2) if only is None else None
+    e2e = _e2e(torch, dg, S, dev, stream, args, l2) if only is None and not args.cases else None
 
     launches = args.steps * R * n_cases
     res = {
@@ -466,6 +489,8 @@ def main():
     ap.add_argument("--sweep-only", action="store_true", help="only the headline sweep (no other ops)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="profiling: one sweep shape 'M,N,K' (no other ops, no e2e)")
+    ap.add_argument("--cases", default="", help="profiling: regex over case ids such as 'moe_w2/M16' or "
+                    "'head_fp8_argmax/M8/N248320/K4096' (only matching cases are built and timed)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

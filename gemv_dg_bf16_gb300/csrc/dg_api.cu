@@ -124,15 +124,19 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
         out->params[0] = M == 4 ? 4 : (M <= 3 ? 8 : 4);
         out->params[1] = M <= 4 ? 4 : 8;
         break;
+    // MoE: [1] warps per CTA, [3] N-tile (W1: gate/up columns, W2: output rows),
+    // [4] pairs per pass -- the GB300 dg_sweep picks per row bucket.
     case DG_OP_MOE_W1:
         out->params[0] = 4;
         out->params[1] = 8;
-        out->params[3] = M <= 1 ? 32 : 64;   // gate/up columns per work unit
+        out->params[3] = M <= 1 ? 32 : (M <= 2 ? 64 : 0);
+        out->params[4] = M <= 2 ? 4 : 2;
         break;
     case DG_OP_MOE_W2:
         out->params[0] = 4;
-        out->params[1] = 4;
-        out->params[3] = M <= 8 ? 64 : 128;  // output rows per work unit
+        out->params[1] = M <= 2 ? 8 : 4;
+        out->params[3] = M <= 1 ? 64 : (M <= 2 ? 128 : (M <= 4 ? 0 : 64));
+        out->params[4] = M <= 1 ? 1 : 2;
         break;
     default:
         break;
@@ -491,9 +495,11 @@ static dg_status launch_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, 
     if (tile == 0) tile = w1 ? wpc * 2 : (wpc * 4 < 32 ? 32 : wpc * 4);
     a.tile = tile;
     if (!w1 && moe_tickets(a.M, a.Nout, tile) > kWsMaxCounters) return DG_ERR_BAD_VARIANT;
-    const void* fn = w1 ? moe_w1_kernel() : moe_w2_kernel();
+    const int mtmax = c.params[4] > 0 ? c.params[4] : 2;
+    const void* fn = w1 ? moe_w1_kernel(mtmax) : moe_w2_kernel(mtmax);
+    if (!fn) return DG_ERR_BAD_VARIANT;
     const int threads = wpc * 32;
-    const size_t smem = static_cast<size_t>(8) * a.K * 2;
+    const size_t smem = static_cast<size_t>(mtmax) * a.K * 2;
     if (smem > kMaxDynSmem) return DG_ERR_UNSUPPORTED_SHAPE;
     int occ = occupancy(fn, threads, smem);
     if (occ < 1) return DG_ERR_UNSUPPORTED_SHAPE;

@@ -25,7 +25,6 @@ namespace {
 constexpr int kMoeR = 4;             // rows per warp group
 constexpr int kMoeMaxPairs = 128;    // M * topk
 constexpr int kMoeMaxE = 1024;
-constexpr int kMoeMT = 8;            // pairs per token chunk
 
 struct Route {
     int U;                           // active experts
@@ -194,14 +193,16 @@ __device__ void w2_chunk(const MoeArgs& a, const Route& R, int e, int n_lo, int 
     }
 }
 
-template <bool W1>
+template <bool W1, int MTMAX>
 __device__ void run_chunk(int c, const MoeArgs& a, const Route& R, int e, int lo, int hi, int p0,
                           const uint4* xs, float* terms)
 {
 #define DG_MOE_CASE(MT)                                                       \
     case MT:                                                                  \
-        if constexpr (W1) w1_chunk<MT>(a, R, e, lo, hi, p0, xs);              \
-        else w2_chunk<MT>(a, R, e, lo, hi, p0, xs, terms);                    \
+        if constexpr (MT <= MTMAX) {                                          \
+            if constexpr (W1) w1_chunk<MT>(a, R, e, lo, hi, p0, xs);          \
+            else w2_chunk<MT>(a, R, e, lo, hi, p0, xs, terms);                \
+        }                                                                     \
         break;
     switch (c) {
         DG_MOE_CASE(1) DG_MOE_CASE(2) DG_MOE_CASE(3) DG_MOE_CASE(4)
@@ -211,12 +212,15 @@ __device__ void run_chunk(int c, const MoeArgs& a, const Route& R, int e, int lo
 #undef DG_MOE_CASE
 }
 
-template <bool W1>
-__global__ void __launch_bounds__(256) moe_kernel(MoeArgs a)
+// MTMAX: most (token, slot) pairs of one expert handled in one pass over its rows.
+// An expert with more pairs is walked in several passes (its rows come from L2 again);
+// a small MTMAX keeps registers, and so resident warps, in check.
+template <bool W1, int MTMAX>
+__global__ void __launch_bounds__(256, MTMAX <= 2 ? 3 : 2) moe_kernel(MoeArgs a)
 {
     __shared__ Route R;
     __shared__ int fold_flag;
-    extern __shared__ uint4 xs[];        // [kMoeMT][K/8]
+    extern __shared__ uint4 xs[];        // [MTMAX][K/8]
     pdl_launch_dependents();
     pdl_wait();                          // routing and activations come from earlier kernels
     route_scan(R, a.ids, a.M, a.topk, a.E, a.ws);
@@ -247,12 +251,12 @@ __global__ void __launch_bounds__(256) moe_kernel(MoeArgs a)
         const int e = R.experts[ue];
         const int lo = tile * a.tile, hi = min(rows, lo + a.tile);
         const int pb = R.offs[ue], pe = R.offs[ue + 1];
-        for (int p0 = pb; p0 < pe; p0 += kMoeMT) {
-            const int c = min(kMoeMT, pe - p0);
+        for (int p0 = pb; p0 < pe; p0 += MTMAX) {
+            const int c = min(MTMAX, pe - p0);
             __syncthreads();                               // xs reuse
             stage_rows(xs, a.x, R, p0, c, kv, W1, a.topk, a.K);
             __syncthreads();
-            run_chunk<W1>(c, a, R, e, lo, hi, p0, xs, terms);
+            run_chunk<W1, MTMAX>(c, a, R, e, lo, hi, p0, xs, terms);
         }
         if constexpr (!W1) {
             // Publish this unit's terms, then take a ticket per token of the unit.
@@ -288,7 +292,26 @@ __global__ void __launch_bounds__(256) moe_kernel(MoeArgs a)
 
 }  // namespace
 
-const void* moe_w1_kernel() { return reinterpret_cast<const void*>(&moe_kernel<true>); }
-const void* moe_w2_kernel() { return reinterpret_cast<const void*>(&moe_kernel<false>); }
+const void* moe_w1_kernel(int mtmax)
+{
+    switch (mtmax) {
+    case 1: return reinterpret_cast<const void*>(&moe_kernel<true, 1>);
+    case 2: return reinterpret_cast<const void*>(&moe_kernel<true, 2>);
+    case 4: return reinterpret_cast<const void*>(&moe_kernel<true, 4>);
+    case 8: return reinterpret_cast<const void*>(&moe_kernel<true, 8>);
+    default: return nullptr;
+    }
+}
+
+const void* moe_w2_kernel(int mtmax)
+{
+    switch (mtmax) {
+    case 1: return reinterpret_cast<const void*>(&moe_kernel<false, 1>);
+    case 2: return reinterpret_cast<const void*>(&moe_kernel<false, 2>);
+    case 4: return reinterpret_cast<const void*>(&moe_kernel<false, 4>);
+    case 8: return reinterpret_cast<const void*>(&moe_kernel<false, 8>);
+    default: return nullptr;
+    }
+}
 
 }  // namespace dg

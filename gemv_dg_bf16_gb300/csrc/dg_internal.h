@@ -19,9 +19,9 @@ const void* bulk_kernel_gemv(int mt);
 const void* bulk_kernel_gateup(int mt);
 const void* bulk_kernel_head(int mt);
 
-// MoE kernels (rows per warp fixed per family; tokens per chunk chosen on device).
-const void* moe_w1_kernel();
-const void* moe_w2_kernel();
+// MoE kernels by the most (token, slot) pairs one pass handles (1, 2, 4 or 8).
+const void* moe_w1_kernel(int mtmax);
+const void* moe_w2_kernel(int mtmax);
 
 // tcgen05 family (dg_tc_dense.cu): padded token count, fixed K-split of a shape,
 // workspace bytes, and the launcher (bf16 linear or interleaved gate/up rows).

@@ -204,6 +204,8 @@ std::string check_choice(int op, const dg_choice& c)
     const int R = c.params[0], wpc = c.params[1];
     if (op == DG_OP_MOE_W1 || op == DG_OP_MOE_W2) {
         if (R != 0 && R != 4) return "MoE rows per warp must be 4";
+        const int mt = c.params[4];
+        if (mt != 0 && mt != 1 && mt != 2 && mt != 4 && mt != 8) return "MoE pairs per pass must be 1, 2, 4 or 8";
     } else if (R != 1 && R != 2 && R != 4 && R != 8) {
         return "rows per warp must be 1, 2, 4 or 8";
     }
@@ -211,6 +213,8 @@ std::string check_choice(int op, const dg_choice& c)
     if (wpc < 1 || wpc > 8) return "warps per CTA must be 1..8";
     for (int i = 2; i < 6; ++i)
         if (c.params[i] < 0) return "negative parameter";
+    if (op != DG_OP_MOE_W1 && op != DG_OP_MOE_W2 && (c.params[3] != 0 || c.params[4] != 0))
+        return "unused parameter set";
     return "";
 }
 
@@ -374,7 +378,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 4; }
+int dg_selection_space(void) { return 5; }
 
 const char* dg_build_id(void) { return build_id(); }
 

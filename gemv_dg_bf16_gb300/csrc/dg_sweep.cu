@@ -107,12 +107,15 @@ std::vector<dg_choice> candidates(int op, const dg_choice& def)
     };
     if (def.variant == DG_VAR_TC) {
         for (int st = 2; st <= 8; ++st) add(mk(DG_VAR_TC, st));
-    } else if (op == DG_OP_MOE_W1) {
-        for (int wpc : {4, 8})
-            for (int tile : {0, 8, 32, 64}) add(mk(DG_VAR_CC_WARP, 4, wpc, 0, tile));
-    } else if (op == DG_OP_MOE_W2) {
-        for (int wpc : {4, 8})
-            for (int tile : {0, 64, 128, 256}) add(mk(DG_VAR_CC_WARP, 4, wpc, 0, tile));
+    } else if (op == DG_OP_MOE_W1 || op == DG_OP_MOE_W2) {
+        const bool w1 = op == DG_OP_MOE_W1;
+        for (int mt : {1, 2, 4})
+            for (int wpc : {4, 8})
+                for (int tile : {0, w1 ? 32 : 64, w1 ? 64 : 128}) {
+                    dg_choice c = mk(DG_VAR_CC_WARP, 4, wpc, 0, tile);
+                    c.params[4] = mt;
+                    add(c);
+                }
     } else {
         for (int R : {1, 2, 4, 8})
             for (int wpc : {4, 8}) {

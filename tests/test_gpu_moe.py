@@ -78,12 +78,13 @@ def test_moe_tiles_and_warps_bitwise_identical(cuda_device, moe_w, M):
     y_ref = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2)
     for wpc in (2, 4, 8):
         for tile in (0, 8, 48, 1536):
-            c = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, wpc, 0, tile)
-            a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=c)
-            assert torch.equal(a.view(torch.int16), a_ref.view(torch.int16)), (wpc, tile)
-            c2 = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, wpc, 0, 4 * tile if tile else 0)
-            y = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2, choice=c2)
-            assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (wpc, tile)
+            for mt in (0, 1, 2, 4, 8):
+                c = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, wpc, 0, tile, mt)
+                a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=c)
+                assert torch.equal(a.view(torch.int16), a_ref.view(torch.int16)), (wpc, tile, mt)
+                c2 = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, wpc, 0, 4 * tile if tile else 0, mt)
+                y = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2, choice=c2)
+                assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (wpc, tile, mt)
 
 
 def test_moe_invalid_ids_flag_and_zero(cuda_device, moe_w):
@@ -113,6 +114,24 @@ def test_moe_invalid_ids_flag_and_zero(cuda_device, moe_w):
     ref, bound = O.moe_w2(bits16(a), ids_c, gw.cpu().numpy(), W2q[sel].cpu().numpy(), s2[sel].cpu().numpy())
     exc = T.linear_excess(f64(y), ref, bound)
     assert (exc <= 0).all()
+
+
+def test_moe_many_pairs_on_one_expert(cuda_device):
+    """Every token routes to the same experts: one expert's pairs span several passes."""
+    W1q, s1, W2q, s2 = S.moe_weights(8, 64, 256, 128, device=cuda_device)
+    M = 16
+    x, ids, gw = S.moe_inputs(M, 256, 3, 8, device=cuda_device)
+    ids[:] = torch.tensor([5, 2, 7], dtype=torch.int32, device=cuda_device)
+    for mt in (1, 2, 8):
+        c = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, mt)
+        a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=c)
+        y = dg.dg_moe_w2(a, ids, gw, W2q, s2, choice=c)
+        torch.cuda.synchronize()
+        r = O.moe_w1_silu(bits16(x), ids.cpu().numpy(), W1q.cpu().numpy(), s1.cpu().numpy())
+        exc = T.silu_mul_excess(f64(a), r["g"], r["u"], r["absg"], r["absu"], r["a"])
+        assert (exc <= 0).all(), mt
+        ref, bound = O.moe_w2(bits16(a), ids.cpu().numpy(), gw.cpu().numpy(), W2q.cpu().numpy(), s2.cpu().numpy())
+        assert (T.linear_excess(f64(y), ref, bound) <= 0).all(), mt
 
 
 def test_moe_token_without_valid_slot_gives_zero(cuda_device):
