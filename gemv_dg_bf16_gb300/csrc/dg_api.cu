@@ -127,12 +127,20 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
     // MoE: [1] warps per CTA, [3] N-tile (W1: gate/up columns, W2: output rows),
     // [4] pairs per pass -- the GB300 dg_sweep picks per row bucket.
     case DG_OP_MOE_W1:
+        if (M >= kTcMoeMinRows) {
+            out->variant = DG_VAR_TC;
+            break;
+        }
         out->params[0] = 4;
         out->params[1] = 8;
         out->params[3] = M <= 1 ? 32 : (M <= 2 ? 64 : 0);
         out->params[4] = M <= 2 ? 4 : 2;
         break;
     case DG_OP_MOE_W2:
+        if (M >= kTcMoeMinRows) {
+            out->variant = DG_VAR_TC;
+            break;
+        }
         out->params[0] = 4;
         out->params[1] = M <= 2 ? 8 : 4;
         out->params[3] = M <= 1 ? 64 : (M <= 2 ? 128 : (M <= 4 ? 0 : 64));
@@ -488,6 +496,8 @@ dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, 
 static dg_status launch_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, MoeArgs a,
                             cudaStream_t stream)
 {
+    if (c.variant == DG_VAR_TC) return launch_tc_moe(w1, dev, c, a, stream);
+    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
     const int wpc = c.params[1] > 0 ? c.params[1] : 8;
     if (c.params[0] != 0 && c.params[0] != 4) return DG_ERR_BAD_VARIANT;
     if (wpc < 1 || wpc > 8 || c.params[2] < 0 || c.params[3] < 0) return DG_ERR_BAD_VARIANT;
@@ -528,7 +538,6 @@ dg_status dg_moe_w1_silu(const void* x, const int32_t* topk_ids, const void* W1,
     if (!dev) return s;
     dg_choice c;
     if ((s = resolve_choice(DG_OP_MOE_W1, M, I, K, choice, &c)) != DG_OK) return s;
-    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
     MoeArgs a{};
     a.x = static_cast<const uint16_t*>(x);
     a.ids = topk_ids;
@@ -560,7 +569,6 @@ dg_status dg_moe_w2(const void* a_in, const int32_t* topk_ids, const float* gw, 
     if (!dev) return s;
     dg_choice c;
     if ((s = resolve_choice(DG_OP_MOE_W2, M, Nout, I, choice, &c)) != DG_OK) return s;
-    if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
     MoeArgs a{};
     a.x = static_cast<const uint16_t*>(a_in);
     a.ids = topk_ids;

@@ -23,93 +23,6 @@ namespace dg {
 namespace {
 
 constexpr int kMoeR = 4;             // rows per warp group
-constexpr int kMoeMaxPairs = 128;    // M * topk
-constexpr int kMoeMaxE = 1024;
-
-struct Route {
-    int U;                           // active experts
-    int P;                           // valid pairs
-    int nvalid[16];                  // valid slots per token
-    int16_t experts[kMoeMaxPairs];   // active expert ids, ascending
-    int16_t offs[kMoeMaxPairs + 1];  // pairs of active expert u: [offs[u], offs[u+1])
-    int8_t ptok[kMoeMaxPairs];
-    int8_t pslot[kMoeMaxPairs];
-    int8_t valid[kMoeMaxPairs];
-    int cnt[kMoeMaxE];               // per expert: pair count, then pair offset
-};
-
-// Every CTA computes the same routing tables (deterministic, no atomics on order).
-__device__ void route_scan(Route& R, const int32_t* __restrict__ ids, int M, int topk, int E,
-                           uint8_t* ws)
-{
-    const int P_all = M * topk;
-    for (int e = threadIdx.x; e < E; e += blockDim.x) R.cnt[e] = 0;
-    __syncthreads();
-    for (int i = threadIdx.x; i < P_all; i += blockDim.x) {
-        const int t = i / topk, k = i - t * topk;
-        const int e = ids[i];
-        bool ok = e >= 0 && e < E;
-        for (int j = 0; ok && j < k; ++j)
-            if (ids[t * topk + j] == e) ok = false;
-        R.valid[i] = ok ? 1 : 0;
-        if (ok) atomicAdd(&R.cnt[e], 1);
-        else if (blockIdx.x == 0) set_status(ws, DG_DEVERR_BAD_TOPK_ID);
-    }
-    __syncthreads();
-    // Warp 0: exclusive scans over experts of (count > 0) and count.
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int carry_u = 0, carry_p = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
-            const int c = e < E ? R.cnt[e] : 0;
-            const int a = c > 0 ? 1 : 0;
-            int su = a, sp = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int nu = __shfl_up_sync(kFull, su, o);
-                const int np = __shfl_up_sync(kFull, sp, o);
-                if (lane >= o) {
-                    su += nu;
-                    sp += np;
-                }
-            }
-            const int ex_u = carry_u + su - a, ex_p = carry_p + sp - c;
-            if (e < E) {
-                if (a) {
-                    R.experts[ex_u] = static_cast<int16_t>(e);
-                    R.offs[ex_u] = static_cast<int16_t>(ex_p);
-                }
-                R.cnt[e] = ex_p;    // now the expert's first pair position
-            }
-            carry_u += __shfl_sync(kFull, su, 31);
-            carry_p += __shfl_sync(kFull, sp, 31);
-        }
-        if (lane == 0) {
-            R.U = carry_u;
-            R.P = carry_p;
-            R.offs[carry_u] = static_cast<int16_t>(carry_p);
-        }
-    }
-    __syncthreads();
-    for (int i = threadIdx.x; i < P_all; i += blockDim.x) {
-        if (!R.valid[i]) continue;
-        const int e = ids[i];
-        int rank = 0;
-        for (int j = 0; j < i; ++j)
-            if (R.valid[j] && ids[j] == e) ++rank;
-        const int pos = R.cnt[e] + rank;
-        R.ptok[pos] = static_cast<int8_t>(i / topk);
-        R.pslot[pos] = static_cast<int8_t>(i % topk);
-    }
-    for (int t = threadIdx.x; t < M; t += blockDim.x) {
-        int n = 0;
-        for (int k = 0; k < topk; ++k) n += R.valid[t * topk + k];
-        R.nvalid[t] = n;
-    }
-    __syncthreads();
-}
-
 // Stage `c` activation rows (one per pair, `kv` 16-byte vectors each) into xs.
 __device__ __forceinline__ void stage_rows(uint4* xs, const uint16_t* __restrict__ src,
                                            const Route& R, int p0, int c, int kv, bool w1, int topk,

@@ -38,9 +38,15 @@ size_t tc_head_smem(int K, int stages);
 dg_status launch_tc_head(const DeviceInfo* dev, const dg_choice& c, const void* x, const void* Wq,
                          const float* scale, void* logits, int32_t* argmax, int M, int N, int K, void* ws,
                          size_t ws_bytes, cudaStream_t stream);
+// tcgen05 MoE W1 / W2 (dg_tc_moe.cu).
+struct MoeArgs;
+dg_status launch_tc_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, const MoeArgs& m, cudaStream_t stream);
+
 // Smallest row bucket the fp8 head sends to the tensor cores, and the largest K
 // whose split activations fit in shared memory.
 constexpr int kTcHeadMinRows = 2;
+// Smallest row bucket the MoE calls send to the tensor cores.
+constexpr int kTcMoeMinRows = 8;
 constexpr int kTcHeadMaxK = 8192;
 
 struct DeviceInfo {
@@ -70,7 +76,7 @@ constexpr size_t kMaxDynSmem = 200 * 1024;
 constexpr size_t kXsBudget = 96 * 1024;
 
 // Smallest row bucket the bf16 linear and gate/up send to the tensor cores.
-constexpr int kTcMinRows = 6;
+constexpr int kTcMinRows = 3;
 
 // Compiled default choice for (op, M, N, K).
 void default_choice(dg_op op, int M, int N, int K, dg_choice* out);

@@ -185,8 +185,6 @@ bool valid_bucket(int m)
 std::string check_choice(int op, const dg_choice& c)
 {
     if (c.variant == DG_VAR_TC) {
-        if (op != DG_OP_GEMV_BF16 && op != DG_OP_GATE_UP_SILU && op != DG_OP_HEAD_FP8_ARGMAX)
-            return "no tensor-core variant for this op";
         if (c.params[0] != 0 && (c.params[0] < 2 || c.params[0] > 8)) return "pipeline stages must be 2..8";
         for (int i = 1; i < 6; ++i)
             if (c.params[i] != 0) return "unused tensor-core parameter set";
@@ -378,7 +376,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 5; }
+int dg_selection_space(void) { return 6; }
 
 const char* dg_build_id(void) { return build_id(); }
 

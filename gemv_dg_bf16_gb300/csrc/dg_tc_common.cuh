@@ -1,0 +1,170 @@
+// dg_tc_common.cuh -- small PTX wrappers for the tcgen05 kernels: bounded mbarrier
+// waits, TMA loads, shared-memory matrix descriptors, fp8 MMA and TMEM loads,
+// and the exact hi/lo e4m3 split of bf16 activation rows.
+#pragma once
+
+#include <cuda.h>
+
+#include "dg_common.cuh"
+
+namespace dg {
+namespace tc {
+
+constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s bound on any wait
+
+__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void bar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void bar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bar_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; false (and the CTA's abort flag
+// raised) after kWaitNs or when another role already aborted.
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag)
+{
+    if (bar_try(bar, parity)) return true;
+    unsigned long long t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (uint32_t i = 1;; ++i) {
+        if (bar_try(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*abort_flag) return false;
+            unsigned long long t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            if (t - t0 > kWaitNs) {
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// K-major operand, 128-byte swizzle, 8-row groups 1024 bytes apart, version 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr)
+{
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// kind::f8f6f4 with e4m3 A and B, fp32 accumulate, K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_f8(int n)
+{
+    return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
+        "%13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+          "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Two fp32 -> packed e4m3x2 (first argument in the low byte), round to nearest even.
+__device__ __forceinline__ uint16_t to_e4m3x2(float lo_elem, float hi_elem)
+{
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi_elem), "f"(lo_elem));
+    return d;
+}
+
+// sigma = 2^(7 - floor(log2 m)) for the row maximum m (1 when m is 0 or not finite),
+// kept inside the normal range so that sigma and 1/sigma are exact.
+__device__ __forceinline__ int split_exponent(float m)
+{
+    int e = 0;
+    if (m > 0.0f && m <= 3.0e38f) {
+        frexpf(m, &e);
+        e = 8 - e;
+        e = e > 126 ? 126 : (e < -126 ? -126 : e);
+    }
+    return e;
+}
+
+// One 16-byte chunk (16 elements) of the hi and lo e4m3 rows of a bf16 row
+// scaled by sg (a power of two): hi = e4m3(y), lo = e4m3(y - hi), y = x * sg.
+__device__ __forceinline__ void split_chunk(const uint16_t* row, int k0, int K, float sg, uint4& hi, uint4& lo)
+{
+    uint32_t hw[4] = {0, 0, 0, 0}, lw[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+        float y0 = 0.0f, y1 = 0.0f;
+        if (k0 + j < K) {
+            const uint32_t pair = *reinterpret_cast<const uint32_t*>(row + k0 + j);
+            y0 = bf16_lo(pair) * sg;
+            y1 = bf16_hi(pair) * sg;
+        }
+        const uint16_t h = to_e4m3x2(y0, y1);
+        const float2 hf = e4m3x2_to_f32(h);
+        const uint16_t l = to_e4m3x2(y0 - hf.x, y1 - hf.y);
+        hw[j / 4] |= static_cast<uint32_t>(h) << (16 * ((j / 2) & 1));
+        lw[j / 4] |= static_cast<uint32_t>(l) << (16 * ((j / 2) & 1));
+    }
+    hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+}
+
+// Byte offset of 16-byte chunk c of row r inside a 128-byte-swizzled K-major block
+// (8-row groups of 1024 bytes).
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c)
+{
+    return static_cast<uint32_t>((r / 8) * 1024 + (r % 8) * 128 + ((c ^ (r % 8)) * 16));
+}
+
+}  // namespace tc
+}  // namespace dg

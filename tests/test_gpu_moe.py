@@ -13,6 +13,9 @@ pytestmark = pytest.mark.gpu
 
 E, I, K, TOPK = 128, 1536, 4096, 6
 MOE_M = [1, 2, 4, 8, 16]
+CC = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, 2)
+TC = dg.Choice.make(dg.DG_VAR_TC, 0)
+FAMILIES = {"cc": CC, "tc": TC, "default": None}
 
 
 @pytest.fixture(scope="module")
@@ -40,12 +43,13 @@ def _w2_ref(a, ids, gw, W2q, s2):
     return O.moe_w2(bits16(a), ids_c, gw.cpu().numpy(), w2, sc2)
 
 
+@pytest.mark.parametrize("family", ["cc", "tc"])
 @pytest.mark.parametrize("M", MOE_M)
-def test_moe_w1_full_size(cuda_device, moe_w, M):
+def test_moe_w1_full_size(cuda_device, moe_w, M, family):
     W1q, s1, W2q, s2 = moe_w
     x, ids, gw = S.moe_inputs(M, K, TOPK, E, device=cuda_device)
     ws = dg.workspace(dg.DG_OP_MOE_W1, M, I, K, TOPK)
-    a = dg.dg_moe_w1_silu(x, ids, W1q, s1, ws=ws)
+    a = dg.dg_moe_w1_silu(x, ids, W1q, s1, ws=ws, choice=FAMILIES[family])
     torch.cuda.synchronize()
     r = _w1_ref(x, ids, W1q, s1)
     exc = T.silu_mul_excess(f64(a), r["g"], r["u"], r["absg"], r["absu"], r["a"])
@@ -53,29 +57,43 @@ def test_moe_w1_full_size(cuda_device, moe_w, M):
     assert dg.dg_device_status(ws) == 0
 
 
+@pytest.mark.parametrize("family", ["cc", "tc"])
 @pytest.mark.parametrize("M", MOE_M)
-def test_moe_w2_full_size_on_gpu_activations(cuda_device, moe_w, M):
+def test_moe_w2_full_size_on_gpu_activations(cuda_device, moe_w, M, family):
     W1q, s1, W2q, s2 = moe_w
+    c = FAMILIES[family]
     x, ids, gw = S.moe_inputs(M, K, TOPK, E, device=cuda_device)
     a = dg.dg_moe_w1_silu(x, ids, W1q, s1)
     ws = dg.workspace(dg.DG_OP_MOE_W2, M, K, I, TOPK)
-    y = dg.dg_moe_w2(a, ids, gw, W2q, s2, ws=ws)
+    y = dg.dg_moe_w2(a, ids, gw, W2q, s2, ws=ws, choice=c)
     torch.cuda.synchronize()
     ref, bound = _w2_ref(a, ids, gw, W2q, s2)
     exc = T.linear_excess(f64(y), ref, bound)
     assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
     # repeated calls reuse the workspace tickets and give the same bits
     for _ in range(3):
-        assert torch.equal(dg.dg_moe_w2(a, ids, gw, W2q, s2, ws=ws).view(torch.int16), y.view(torch.int16))
+        assert torch.equal(dg.dg_moe_w2(a, ids, gw, W2q, s2, ws=ws, choice=c).view(torch.int16), y.view(torch.int16))
     assert dg.dg_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("M", [1, 5, 16])
+def test_moe_tc_stages_bitwise_identical(cuda_device, moe_w, M):
+    W1q, s1, W2q, s2 = moe_w
+    x, ids, gw = S.moe_inputs(M, K, TOPK, E, rep=3, device=cuda_device)
+    a_ref = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=TC)
+    y_ref = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2, choice=TC)
+    for st in (2, 3, 5, 8):
+        c = dg.Choice.make(dg.DG_VAR_TC, st)
+        assert torch.equal(dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=c).view(torch.int16), a_ref.view(torch.int16))
+        assert torch.equal(dg.dg_moe_w2(a_ref, ids, gw, W2q, s2, choice=c).view(torch.int16), y_ref.view(torch.int16))
 
 
 @pytest.mark.parametrize("M", [1, 4, 16])
 def test_moe_tiles_and_warps_bitwise_identical(cuda_device, moe_w, M):
     W1q, s1, W2q, s2 = moe_w
     x, ids, gw = S.moe_inputs(M, K, TOPK, E, rep=7, device=cuda_device)
-    a_ref = dg.dg_moe_w1_silu(x, ids, W1q, s1)
-    y_ref = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2)
+    a_ref = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=CC)
+    y_ref = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2, choice=CC)
     for wpc in (2, 4, 8):
         for tile in (0, 8, 48, 1536):
             for mt in (0, 1, 2, 4, 8):
@@ -87,8 +105,10 @@ def test_moe_tiles_and_warps_bitwise_identical(cuda_device, moe_w, M):
                 assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (wpc, tile, mt)
 
 
-def test_moe_invalid_ids_flag_and_zero(cuda_device, moe_w):
+@pytest.mark.parametrize("family", ["cc", "tc"])
+def test_moe_invalid_ids_flag_and_zero(cuda_device, moe_w, family):
     W1q, s1, W2q, s2 = moe_w
+    c = FAMILIES[family]
     M = 3
     x, ids, gw = S.moe_inputs(M, K, TOPK, E, device=cuda_device)
     bad = ids.clone()
@@ -96,13 +116,13 @@ def test_moe_invalid_ids_flag_and_zero(cuda_device, moe_w):
     bad[1, 5] = 500              # out of range
     bad[2, 0] = -3
     ws = dg.workspace(dg.DG_OP_MOE_W1, M, I, K, TOPK)
-    a = dg.dg_moe_w1_silu(x, bad, W1q, s1, ws=ws)
+    a = dg.dg_moe_w1_silu(x, bad, W1q, s1, ws=ws, choice=c)
     assert dg.dg_device_status(ws) & 0x1
     assert (a[0, 2] == 0).all() and (a[1, 5] == 0).all() and (a[2, 0] == 0).all()
     dg.dg_device_status_clear(ws)
     assert dg.dg_device_status(ws) == 0
     ws2 = dg.workspace(dg.DG_OP_MOE_W2, M, K, I, TOPK)
-    y = dg.dg_moe_w2(a, bad, gw, W2q, s2, ws=ws2)
+    y = dg.dg_moe_w2(a, bad, gw, W2q, s2, ws=ws2, choice=c)
     torch.cuda.synchronize()
     assert dg.dg_device_status(ws2) & 0x1
     # the oracle skips the same slots
@@ -122,8 +142,8 @@ def test_moe_many_pairs_on_one_expert(cuda_device):
     M = 16
     x, ids, gw = S.moe_inputs(M, 256, 3, 8, device=cuda_device)
     ids[:] = torch.tensor([5, 2, 7], dtype=torch.int32, device=cuda_device)
-    for mt in (1, 2, 8):
-        c = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, mt)
+    for c in [dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, mt) for mt in (1, 2, 8)] + [TC]:
+        mt = c.params[4]
         a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=c)
         y = dg.dg_moe_w2(a, ids, gw, W2q, s2, choice=c)
         torch.cuda.synchronize()
@@ -134,24 +154,26 @@ def test_moe_many_pairs_on_one_expert(cuda_device):
         assert (T.linear_excess(f64(y), ref, bound) <= 0).all(), mt
 
 
-def test_moe_token_without_valid_slot_gives_zero(cuda_device):
+@pytest.mark.parametrize("family", ["cc", "tc"])
+def test_moe_token_without_valid_slot_gives_zero(cuda_device, family):
     W1q, s1, W2q, s2 = S.moe_weights(8, 64, 256, 128, device=cuda_device)
     x, ids, gw = S.moe_inputs(2, 256, 3, 8, device=cuda_device)
     ids[1] = -1
-    a = dg.dg_moe_w1_silu(x, ids, W1q, s1)
-    y = dg.dg_moe_w2(a, ids, gw, W2q, s2)
+    a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=FAMILIES[family])
+    y = dg.dg_moe_w2(a, ids, gw, W2q, s2, choice=FAMILIES[family])
     torch.cuda.synchronize()
     assert (y[1] == 0).all() and (a[1] == 0).all()
     assert (y[0] != 0).any()
 
 
-def test_moe_single_expert_equals_scaled_gemv(cuda_device):
+@pytest.mark.parametrize("family", ["cc", "tc"])
+def test_moe_single_expert_equals_scaled_gemv(cuda_device, family):
     """One token, one slot, gate weight 1: W2 reduces to a per-row-scaled fp8 GEMV."""
     W1q, s1, W2q, s2 = S.moe_weights(4, 512, 1024, 768, device=cuda_device)
     a = torch.randn((1, 1, 512), generator=torch.Generator().manual_seed(2)).to(torch.bfloat16).to(cuda_device)
     ids = torch.tensor([[2]], dtype=torch.int32, device=cuda_device)
     gw = torch.ones((1, 1), dtype=torch.float32, device=cuda_device)
-    y = dg.dg_moe_w2(a, ids, gw, W2q, s2)
+    y = dg.dg_moe_w2(a, ids, gw, W2q, s2, choice=FAMILIES[family])
     torch.cuda.synchronize()
     lg, ad = O.head_fp8(bits16(a[0]), W2q[2].cpu().numpy(), 1.0)
     s = s2[2].cpu().numpy().astype(np.float64)

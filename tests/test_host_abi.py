@@ -88,7 +88,8 @@ def test_select_defaults_and_bucket_padding():
             c = dg.dg_select(op, M, 4096, 4096)
             dense_bf16 = op in (dg.DG_OP_GEMV_BF16, dg.DG_OP_GATE_UP_SILU)
             head = op == dg.DG_OP_HEAD_FP8_ARGMAX
-            want = dg.DG_VAR_TC if (dense_bf16 and M >= 5) or (head and M >= 2) else dg.DG_VAR_CC_WARP
+            moe = op in (dg.DG_OP_MOE_W1, dg.DG_OP_MOE_W2)
+            want = dg.DG_VAR_TC if (dense_bf16 and M >= 3) or (head and M >= 2) or (moe and M >= 7) else dg.DG_VAR_CC_WARP
             assert c.variant == want and c.from_table == 0, (op, M, c)
     with pytest.raises(dg.DGError):
         dg.dg_select(0, 129, 4096, 4096)
