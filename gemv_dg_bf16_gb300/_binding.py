@@ -17,6 +17,10 @@ _LIBPATH = os.path.join(_HERE, "libdecodegemm.so")
 
 DG_OP_GEMV_BF16, DG_OP_GATE_UP_SILU, DG_OP_HEAD_FP8_ARGMAX, DG_OP_MOE_W1, DG_OP_MOE_W2 = range(5)
 DG_VAR_DEFAULT, DG_VAR_CC_WARP, DG_VAR_CC_BULK, DG_VAR_TC = range(4)
+(DG_OK, DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_UNSUPPORTED_SHAPE, DG_ERR_WORKSPACE_TOO_SMALL, DG_ERR_CUDA,
+ DG_ERR_TABLE_REFUSED, DG_ERR_NO_DEVICE, DG_ERR_BAD_VARIANT) = range(9)
+DG_DEVERR_BAD_TOPK_ID = 0x1
+DG_DEVERR_WAIT_TIMEOUT = 0x2
 
 
 def _rows_buckets():
@@ -81,6 +85,8 @@ def lib():
     L.dg_workspace_bytes.restype = Z
     L.dg_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int32), P]
     L.dg_device_status_clear.argtypes = [P, P]
+    L.dg_selftest_wait_timeout.argtypes = [P, I, P]
+    L.dg_selftest_wait_timeout.restype = S
     L.dg_set_launch_flags.argtypes = [ctypes.c_uint]
     L.dg_set_launch_flags.restype = S
     L.dg_launch_flags.argtypes = []
@@ -155,6 +161,10 @@ def dg_set_launch_flags(flags: int):
 
 def dg_launch_flags() -> int:
     return int(lib().dg_launch_flags())
+
+
+def dg_selftest_wait_timeout(ws, timeout_us: int = 20000, stream=None):
+    _ok(lib().dg_selftest_wait_timeout(_ptr(ws), int(timeout_us), _stream(stream)), "dg_selftest_wait_timeout")
 
 
 def dg_workspace_bytes(op: int, M: int, N: int, K: int, topk: int = 0) -> int:

@@ -43,8 +43,9 @@ __device__ __forceinline__ bool bar_try(uint32_t bar, uint32_t parity)
 }
 
 // Wait for the phase of `parity` to complete; false (and the CTA's abort flag
-// raised) after kWaitNs or when another role already aborted.
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag)
+// raised) after `limit_ns` or when another role already aborted.
+__device__ __forceinline__ bool bar_wait_for(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned long long limit_ns)
 {
     if (bar_try(bar, parity)) return true;
     unsigned long long t0;
@@ -55,12 +56,17 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile
             if (*abort_flag) return false;
             unsigned long long t;
             asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-            if (t - t0 > kWaitNs) {
+            if (t - t0 > limit_ns) {
                 *abort_flag = 1;
                 return false;
             }
         }
     }
+}
+
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag)
+{
+    return bar_wait_for(bar, parity, abort_flag, kWaitNs);
 }
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar)

@@ -141,6 +141,12 @@ unsigned dg_launch_flags(void);
 /* Clear the device status word (asynchronous on `stream`). */
 dg_status dg_device_status_clear(void* ws, dg_stream_t stream);
 
+/* Health check of the bounded waits (no counterpart on the pages): one CTA waits on a barrier that never completes, gives up
+ * after timeout_us (1 .. 2,000,000) and sets DG_DEVERR_WAIT_TIMEOUT in the
+ * workspace status word -- the same path every pipelined kernel takes when a wait
+ * runs out.  Asynchronous on `stream`; the context stays usable. */
+dg_status dg_selftest_wait_timeout(void* ws, int timeout_us, dg_stream_t stream);
+
 /* ---------------------------------------------------------------- compute */
 
 /* Decode linear, mstar PR #1104 (decode GEMM table), "Why" / "What changed":

@@ -1,0 +1,147 @@
+"""Every entry point captured into a CUDA graph and replayed: the replay gives the
+same bits as an eager call on the same inputs, repeated replays reuse the
+workspace tickets correctly, and nothing in a call synchronises the host."""
+import pytest
+import torch
+
+import gemv_dg_bf16_gb300 as dg
+from synth import decode_inputs as S
+
+pytestmark = pytest.mark.gpu
+
+TC = dg.Choice.make(dg.DG_VAR_TC, 0)
+CC = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0)
+CC_MOE = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, 2)
+
+
+def _bits(t):
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+
+def _graph_matches_eager(run, make_inputs, replays=3):
+    """run(inputs) writes into static outputs and returns them; make_inputs(seed)
+    returns a list of tensors with the shapes of the captured inputs."""
+    static_in = [t.clone() for t in make_inputs(0)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run(static_in)                       # lazy library set-up happens outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        outs = run(static_in)
+    for seed in range(1, replays + 1):
+        fresh = make_inputs(seed)
+        for s, f in zip(static_in, fresh):
+            s.copy_(f)
+        g.replay()
+        torch.cuda.synchronize()
+        got = [_bits(o).clone() for o in outs]
+        want = [_bits(o).clone() for o in run([t.clone() for t in fresh])]
+        torch.cuda.synchronize()
+        for a, b in zip(got, want):
+            assert torch.equal(a, b), f"replay {seed} differs from the eager call"
+
+
+@pytest.mark.parametrize("choice", [None, CC, TC], ids=["default", "cc", "tc"])
+@pytest.mark.parametrize("M", [1, 4, 16, 64])
+def test_gemv_graph_replay(cuda_device, M, choice):
+    N, K = 1536, 2048
+    W = S.linear_inputs(M, N, K, device=cuda_device)[1]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K)
+
+    def make(seed):
+        return [S.normal_bf16((M, K), 1.0, 1000 + seed, device=cuda_device)]
+
+    def run(inp):
+        return [dg.dg_gemv_bf16(inp[0], W, y=y, ws=ws, choice=choice)]
+
+    _graph_matches_eager(run, make)
+    assert dg.dg_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("choice", [None, CC, TC], ids=["default", "cc", "tc"])
+@pytest.mark.parametrize("M", [2, 8, 32])
+def test_gate_up_graph_replay(cuda_device, M, choice):
+    Nh, K = 768, 2048
+    W = S.gate_up_inputs(M, Nh, K, device=cuda_device)[1]
+    out = torch.empty((M, Nh), dtype=torch.bfloat16, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GATE_UP_SILU, M, Nh, K)
+
+    def make(seed):
+        return [S.normal_bf16((M, K), 1.0, 2000 + seed, device=cuda_device)]
+
+    def run(inp):
+        return [dg.dg_gate_up_silu(inp[0], W, out=out, ws=ws, choice=choice)]
+
+    _graph_matches_eager(run, make)
+
+
+@pytest.mark.parametrize("choice", [None, CC, TC], ids=["default", "cc", "tc"])
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_head_graph_replay(cuda_device, M, choice):
+    N, K = 20000, 2048
+    _, Wq, scale = S.head_inputs(M, N, K, device=cuda_device)
+    logits = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_device)
+    am = torch.empty((M,), dtype=torch.int32, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_HEAD_FP8_ARGMAX, M, N, K)
+    if choice is TC and M < 2:
+        pytest.skip("the tensor-core head starts at two rows")
+
+    def make(seed):
+        return [S.normal_bf16((M, K), 1.0, 3000 + seed, device=cuda_device)]
+
+    def run(inp):
+        lg, a = dg.dg_head_fp8_argmax(inp[0], Wq, scale, logits=logits, argmax=am, ws=ws, choice=choice)
+        return [lg, a]
+
+    _graph_matches_eager(run, make)
+    assert dg.dg_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("choice", [None, CC_MOE, TC], ids=["default", "cc", "tc"])
+@pytest.mark.parametrize("M", [1, 8])
+def test_moe_graph_replay(cuda_device, M, choice):
+    E, I, K, topk = 16, 512, 1024, 4
+    W1q, s1, W2q, s2 = S.moe_weights(E, I, K, K, device=cuda_device)
+    a = torch.empty((M, topk, I), dtype=torch.bfloat16, device=cuda_device)
+    y = torch.empty((M, K), dtype=torch.bfloat16, device=cuda_device)
+    ws1 = dg.workspace(dg.DG_OP_MOE_W1, M, I, K, topk)
+    ws2 = dg.workspace(dg.DG_OP_MOE_W2, M, K, I, topk)
+
+    def make(seed):
+        x, ids, gw = S.moe_inputs(M, K, topk, E, rep=seed, device=cuda_device)
+        return [x, ids, gw]
+
+    def run(inp):
+        dg.dg_moe_w1_silu(inp[0], inp[1], W1q, s1, a=a, ws=ws1, choice=choice)
+        dg.dg_moe_w2(a, inp[1], inp[2], W2q, s2, y=y, ws=ws2, choice=choice)
+        return [a, y]
+
+    _graph_matches_eager(run, make)
+    assert dg.dg_device_status(ws1) == 0 and dg.dg_device_status(ws2) == 0
+
+
+def test_calls_do_not_synchronise(cuda_device):
+    """With preallocated outputs and workspaces no entry point blocks the host."""
+    M, N, K = 4, 1024, 1024
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_HEAD_FP8_ARGMAX, M, 8192, K)
+    _, Wq, scale = S.head_inputs(M, 8192, K, device=cuda_device)
+    lg = torch.empty((M, 8192), dtype=torch.bfloat16, device=cuda_device)
+    am = torch.empty((M,), dtype=torch.int32, device=cuda_device)
+    dg.dg_gemv_bf16(x, W, y=y, ws=ws)
+    dg.dg_head_fp8_argmax(x, Wq, scale, logits=lg, argmax=am, ws=ws)
+    torch.cuda.synchronize()
+    prev = torch.cuda.get_sync_debug_mode()
+    torch.cuda.set_sync_debug_mode("error")
+    try:
+        for _ in range(3):
+            dg.dg_gemv_bf16(x, W, y=y, ws=ws)
+            dg.dg_head_fp8_argmax(x, Wq, scale, logits=lg, argmax=am, ws=ws)
+    finally:
+        torch.cuda.set_sync_debug_mode(prev)
+    torch.cuda.synchronize()

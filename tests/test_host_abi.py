@@ -189,3 +189,13 @@ def test_force_knob_drives_select():
                             "print(dg.lib().dg_select(0, 3, 64, 64, dg._binding.ctypes.byref(dg.Choice())))")
     out = subprocess.run([sys.executable, "-c", code_bad], env=env, capture_output=True, text=True, check=True).stdout
     assert out.strip() == "8"
+
+
+def test_binding_constants_match_header():
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "dg.h")).read()
+    enums = dict((k, int(v)) for k, v in re.findall(r"\b(DG_(?:OK|ERR_\w+))\s*=\s*(\d+)", hdr))
+    defines = dict((k, int(v, 16)) for k, v in re.findall(r"#define\s+(DG_DEVERR_\w+)\s+0x([0-9A-Fa-f]+)", hdr))
+    assert len(enums) == 9 and len(defines) == 2
+    for name, val in {**enums, **defines}.items():
+        assert getattr(dg, name) == val, name
