@@ -1,6 +1,6 @@
 // dg_tc_dense.cu -- tcgen05 tensor-core family (DG_VAR_TC) for the bf16 linear and
-// the fused gate/up + SiLU.mul at M >= 16 (here the contraction is dense enough
-// that CUDA-core FMA throughput, not HBM, would bound it).
+// the fused gate/up + SiLU.mul (the default from three token rows up, where the
+// CUDA-core FMA and bf16-unpack work per weight byte would start to bound it).
 //
 // Swap-AB: a CTA owns a tile of 128 weight rows (the MMA's M) and one fixed K
 // range; the tokens are the MMA's N (M padded to MP in {16, 32, 64, 128}), so
@@ -28,8 +28,8 @@
 #include <cstdio>
 #include <mutex>
 
-#include "dg_common.cuh"
 #include "dg_internal.h"
+#include "dg_tc_common.cuh"
 
 namespace dg {
 namespace {
@@ -39,7 +39,6 @@ constexpr int kKB = 64;                           // K per stage: one 128-byte s
 constexpr int kWBox = kTileRows * kKB * 2;        // 16 KB
 constexpr int kThreads = 192;
 constexpr int kMaxCluster = 8;                    // portable thread-block cluster size
-constexpr unsigned long long kWaitNs = 2000000000ull;   // 2 s bound on any wait
 
 struct TcArgs {
     int N, K, M;
@@ -49,117 +48,6 @@ struct TcArgs {
     int ld_out;
     uint8_t* ws;          // status word only (the K-split fold stays on chip)
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p)
-{
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer()
-{
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
-{
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes)
-{
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait; returns false (and raises the CTA's abort flag) on timeout.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag)
-{
-    if (mbar_try(bar, parity)) return true;
-    const unsigned long long t0 = globaltimer();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitNs) {
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-        : "memory");
-}
-
-// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row
-// groups 1024 bytes apart (stride byte offset), descriptor version 1.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
-    d |= static_cast<uint64_t>(1) << 16;              // leading byte offset (unused for this layout)
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;       // stride byte offset
-    d |= static_cast<uint64_t>(1) << 46;               // version
-    d |= static_cast<uint64_t>(2) << 61;               // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major,
-// N = mp, M = 128.
-__host__ __device__ constexpr uint32_t mma_idesc(int mp)
-{
-    return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(mp >> 3) << 17) |
-           (static_cast<uint32_t>(kTileRows >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(tmem_d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, "
-        "%13, %14, %15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
-          "=r"(v[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 
 // Every thread of every CTA of the cluster executes this, unconditionally.
 __device__ __forceinline__ void cluster_sync_all()
@@ -239,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kXBox = MP * kKB * 2;
     constexpr int kStage = kWBox + kXBox;
     constexpr uint32_t kCols = MP < 32 ? 32 : MP;
-    constexpr uint32_t kIdesc = mma_idesc(MP);
+    constexpr uint32_t kIdesc = tc::idesc_bf16(MP);
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -257,13 +145,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkb = kb1 - kb0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2 * S + 1; ++s) mbar_init(smem_u32(bars + s), 1);
+        for (int s = 0; s < 2 * S + 1; ++s) tc::bar_init(tc::su32(bars + s), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tc::su32(tmem_holder)),
                      "r"(kCols));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
@@ -272,31 +160,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (clustered) cluster_sync_all();     // every rank's barriers exist before any remote access
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_holder;
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S), accum = smem_u32(bars + 2 * S);
+    const uint32_t full0 = tc::su32(bars), empty0 = tc::su32(bars + S), accum = tc::su32(bars + 2 * S);
 
     pdl_launch_dependents();
     if (warp == 0) {
         if (lane == 0) {
             // Weight boxes of the first ring fill do not depend on earlier kernels:
             // issue them before waiting, the activation boxes after.
+            // Weights are read once: they are the first lines evicted from L2.
+            const uint64_t once = tc::policy_evict_first();
             const int pre = nkb < S ? nkb : S;
             for (int i = 0; i < pre; ++i) {
-                const uint32_t dst = smem_u32(smem + i * kStage);
-                mbar_expect_tx(full0 + 8 * i, kStage);
-                tma_load_2d(dst, &tmW, (kb0 + i) * kKB, tile * kTileRows, full0 + 8 * i);
+                const uint32_t dst = tc::su32(smem + i * kStage);
+                tc::bar_expect_tx(full0 + 8 * i, kStage);
+                tc::tma_2d_hint(dst, &tmW, (kb0 + i) * kKB, tile * kTileRows, full0 + 8 * i, once);
             }
             pdl_wait();
             for (int i = 0; i < pre; ++i)
-                tma_load_2d(smem_u32(smem + i * kStage) + kWBox, &tmX, (kb0 + i) * kKB, 0, full0 + 8 * i);
+                tc::tma_2d(tc::su32(smem + i * kStage) + kWBox, &tmX, (kb0 + i) * kKB, 0, full0 + 8 * i);
             for (int i = pre; i < nkb; ++i) {
                 const int s = i % S;
                 const uint32_t round = static_cast<uint32_t>(i / S);
-                if (!mbar_wait(empty0 + 8 * s, (round & 1u) ^ 1u, abort_flag)) break;
-                const uint32_t dst = smem_u32(smem + s * kStage);
-                mbar_expect_tx(full0 + 8 * s, kStage);
+                if (!tc::bar_wait(empty0 + 8 * s, (round & 1u) ^ 1u, abort_flag)) break;
+                const uint32_t dst = tc::su32(smem + s * kStage);
+                tc::bar_expect_tx(full0 + 8 * s, kStage);
                 const int k = (kb0 + i) * kKB;
-                tma_load_2d(dst, &tmW, k, tile * kTileRows, full0 + 8 * s);
-                tma_load_2d(dst + kWBox, &tmX, k, 0, full0 + 8 * s);
+                tc::tma_2d_hint(dst, &tmW, k, tile * kTileRows, full0 + 8 * s, once);
+                tc::tma_2d(dst + kWBox, &tmX, k, 0, full0 + 8 * s);
             }
         } else {
             pdl_wait();
@@ -307,16 +197,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < nkb; ++i) {
                 const int s = i % S;
                 const uint32_t round = static_cast<uint32_t>(i / S);
-                if (!mbar_wait(full0 + 8 * s, round & 1u, abort_flag)) break;
+                if (!tc::bar_wait(full0 + 8 * s, round & 1u, abort_flag)) break;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t wa = smem_u32(smem + s * kStage), xa = wa + kWBox;
+                const uint32_t wa = tc::su32(smem + s * kStage), xa = wa + kWBox;
 #pragma unroll
                 for (int kk = 0; kk < kKB / 16; ++kk)
-                    mma_bf16(tmem, smem_desc(wa + kk * 32), smem_desc(xa + kk * 32), kIdesc,
+                    tc::mma_bf16(tmem, tc::sw128_desc(wa + kk * 32), tc::sw128_desc(xa + kk * 32), kIdesc,
                              (i > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(empty0 + 8 * s);
+                tc::commit(empty0 + 8 * s);
             }
-            mma_commit(accum);           // fires once every MMA issued above has completed
+            tc::commit(accum);           // fires once every MMA issued above has completed
         }
     } else {
         pdl_wait();
@@ -324,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         const int row = q * 32 + lane;
         const int n = tile * kTileRows + row;
-        const bool ok = mbar_wait(accum, 0, abort_flag);
+        const bool ok = tc::bar_wait(accum, 0, abort_flag);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         if (!ok || *abort_flag) {
             if (row == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
@@ -332,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < MP / 16; ++c) {
                 uint32_t v[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
+                tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     const int t = c * 16 + j;
@@ -345,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
             for (int c = 0; c < MP / 16; ++c) {
                 uint32_t v[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
+                tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) P[(c * 16 + j) * kTileRows + row] = __uint_as_float(v[j]);
             }
@@ -362,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int hi = ((split + 1) * (kTileRows / 4) / a.nsplit) * 4;
             const int w4 = (hi - lo) / 4;
             const int count = w4 * a.M;
-            const uint32_t pbase = smem_u32(smem);
+            const uint32_t pbase = tc::su32(smem);
             uint32_t peer[kMaxCluster];
 #pragma unroll
             for (int r = 0; r < kMaxCluster; ++r) peer[r] = r < a.nsplit ? map_to_rank(pbase, r) : 0u;

@@ -27,8 +27,8 @@
 
 #include <mutex>
 
-#include "dg_common.cuh"
 #include "dg_internal.h"
+#include "dg_tc_common.cuh"
 
 namespace dg {
 namespace {
@@ -40,7 +40,6 @@ constexpr int kTokens = 8;                 // token rows per launch
 constexpr int kBRows = 2 * kTokens;        // hi + lo rows (MMA N)
 constexpr int kXBlock = kBRows * kKB;      // 2 KB of split activations per k-block
 constexpr int kThreads = 192;
-constexpr unsigned long long kWaitNs = 2000000000ull;
 
 struct HeadArgs {
     int N, K, M;
@@ -52,76 +51,8 @@ struct HeadArgs {
     uint8_t* ws;
 };
 
-__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-
-__device__ __forceinline__ bool try_wait(uint32_t bar, uint32_t parity)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, volatile int* abort_flag)
-{
-    if (try_wait(bar, parity)) return true;
-    unsigned long long t0;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    for (uint32_t i = 1;; ++i) {
-        if (try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0) {
-            if (*abort_flag) return false;
-            unsigned long long t;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-            if (t - t0 > kWaitNs) {
-                *abort_flag = 1;
-                return false;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr)
-{
-    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
-           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
-           (static_cast<uint64_t>(2) << 61);
-}
-
-// kind::f8f6f4 instruction descriptor: fp32 accumulate, A and B e4m3 (format 0),
-// both K-major, N = 16, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | (static_cast<uint32_t>(kBRows >> 3) << 17) |
-                            (static_cast<uint32_t>(kRows >> 4) << 24);
-
-__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d), "l"(a), "l"(b), "r"(kIdesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ void commit(uint32_t bar)
-{
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-// Two fp32 -> packed e4m3x2 (first argument in the low byte), round to nearest even.
-__device__ __forceinline__ uint16_t to_e4m3x2(float lo_elem, float hi_elem)
-{
-    uint16_t d;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi_elem), "f"(lo_elem));
-    return d;
-}
-
-__device__ __forceinline__ float2 from_e4m3x2(uint16_t v) { return e4m3x2_to_f32(v); }
+// kind::f8f6f4 instruction descriptor: e4m3 A and B, fp32 accumulate, N = 16, M = 128.
+constexpr uint32_t kIdesc = tc::idesc_f8(kBRows);
 
 __global__ void __launch_bounds__(kThreads, 1)
     tc_head_kernel(const __grid_constant__ CUtensorMap tmW, HeadArgs a)
@@ -142,24 +73,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ int last_sh;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t full0 = su32(bars), empty0 = su32(bars + S), accf0 = su32(bars + 2 * S),
-                   acce0 = su32(bars + 2 * S + 2);
+    const uint32_t full0 = tc::su32(bars), empty0 = tc::su32(bars + S), accf0 = tc::su32(bars + 2 * S),
+                   acce0 = tc::su32(bars + 2 * S + 2);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(full0 + 8 * s));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(empty0 + 8 * s));
+            tc::bar_init(full0 + 8 * s, 1);
+            tc::bar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; ++b) {
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(accf0 + 8 * b));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;" ::"r"(acce0 + 8 * b));
+            tc::bar_init(accf0 + 8 * b, 1);
+            tc::bar_init(acce0 + 8 * b, 4);
         }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(su32(tmem_holder)));
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 32;" ::"r"(tc::su32(tmem_holder)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -175,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------------ producer
         if (lane == 0) {
+            const uint64_t once = tc::policy_evict_first();   // weights are read exactly once
             int i = 0;
             bool stop = false;
             for (int jt = 0; jt < my_tiles && !stop; ++jt) {
@@ -182,18 +114,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < a.nkb; ++kb, ++i) {
                     const int s = i % S;
                     const uint32_t round = static_cast<uint32_t>(i / S);
-                    if (!wait(empty0 + 8 * s, (round & 1u) ^ 1u, abort_flag)) {
+                    if (!tc::bar_wait(empty0 + 8 * s, (round & 1u) ^ 1u, abort_flag)) {
                         stop = true;
                         break;
                     }
-                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(full0 + 8 * s),
-                                 "r"(kWBox)
-                                 : "memory");
-                    asm volatile(
-                        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-                        "%3}], [%4];" ::"r"(su32(wst + s * kWBox)),
-                        "l"(reinterpret_cast<uint64_t>(&tmW)), "r"(kb * kKB), "r"(tile * kRows), "r"(full0 + 8 * s)
-                        : "memory");
+                    tc::bar_expect_tx(full0 + 8 * s, kWBox);
+                    tc::tma_2d_hint(tc::su32(wst + s * kWBox), &tmW, kb * kKB, tile * kRows, full0 + 8 * s, once);
                 }
             }
         }
@@ -220,12 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float m = 0.0f;
             for (int w = 0; w < 5; ++w) m = fmaxf(m, redmax[w][t160]);
             // sigma = 2^(7 - floor(log2 m)); the scaled maximum lies in [128, 256).
-            int e = 0;
-            if (m > 0.0f && m <= 3.0e38f) {
-                frexpf(m, &e);                                  // m = f * 2^e, f in [0.5, 1)
-                e = 8 - e;
-                e = e > 126 ? 126 : (e < -126 ? -126 : e);      // sigma and 1/sigma stay normal
-            }
+            const int e = tc::split_exponent(m);
             inv_sigma[t160] = ldexpf(1.0f, -e);
             redmax[0][t160] = ldexpf(1.0f, e);                   // sigma itself
         }
@@ -236,31 +157,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int chunks = a.nkb * kTokens * 8;                  // (kb, token, chunk)
         for (int q = t160; q < chunks; q += 160) {
             const int c = q & 7, t = (q >> 3) % kTokens, kb = q / (8 * kTokens);
-            uint32_t hw[4] = {0, 0, 0, 0}, lw[4] = {0, 0, 0, 0};
-            if (t < a.M) {
-                const float sg = redmax[0][t];
-                const int k0 = kb * kKB + c * 16;
-#pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    float y0 = 0.0f, y1 = 0.0f;
-                    if (k0 + j < a.K) {
-                        const uint32_t pair = *reinterpret_cast<const uint32_t*>(a.x + static_cast<size_t>(t) * a.K + k0 + j);
-                        y0 = bf16_lo(pair) * sg;
-                        y1 = bf16_hi(pair) * sg;
-                    }
-                    const uint16_t h = to_e4m3x2(y0, y1);
-                    const float2 hf = from_e4m3x2(h);
-                    const uint16_t l = to_e4m3x2(y0 - hf.x, y1 - hf.y);
-                    hw[j / 4] |= static_cast<uint32_t>(h) << (16 * ((j / 2) & 1));
-                    lw[j / 4] |= static_cast<uint32_t>(l) << (16 * ((j / 2) & 1));
-                }
-            }
+            uint4 hi = make_uint4(0u, 0u, 0u, 0u), lo = hi;
+            if (t < a.M) tc::split_chunk(a.x + static_cast<size_t>(t) * a.K, kb * kKB + c * 16, a.K, redmax[0][t], hi, lo);
             uint8_t* blk = xsplit + kb * kXBlock;
-            const int rh = t, rl = kTokens + t;
-            *reinterpret_cast<uint4*>(blk + (rh / 8) * 1024 + (rh % 8) * 128 + ((c ^ (rh % 8)) * 16)) =
-                make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(blk + (rl / 8) * 1024 + (rl % 8) * 128 + ((c ^ (rl % 8)) * 16)) =
-                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            *reinterpret_cast<uint4*>(blk + tc::sw128_offset(t, c)) = hi;
+            *reinterpret_cast<uint4*>(blk + tc::sw128_offset(kTokens + t, c)) = lo;
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // generic writes -> MMA reads
         asm volatile("bar.sync 1, 160;" ::: "memory");
@@ -273,24 +174,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int jt = 0; jt < my_tiles && !stop; ++jt) {
                     const int b = jt & 1;
                     const uint32_t use = static_cast<uint32_t>(jt >> 1);
-                    if (!wait(acce0 + 8 * b, (use & 1u) ^ 1u, abort_flag)) break;
+                    if (!tc::bar_wait(acce0 + 8 * b, (use & 1u) ^ 1u, abort_flag)) break;
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                     const uint32_t d = tmem + static_cast<uint32_t>(b * kBRows);
                     for (int kb = 0; kb < a.nkb; ++kb, ++i) {
                         const int s = i % S;
                         const uint32_t round = static_cast<uint32_t>(i / S);
-                        if (!wait(full0 + 8 * s, round & 1u, abort_flag)) {
+                        if (!tc::bar_wait(full0 + 8 * s, round & 1u, abort_flag)) {
                             stop = true;
                             break;
                         }
                         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                        const uint32_t wa = su32(wst + s * kWBox), xa = su32(xsplit + kb * kXBlock);
+                        const uint32_t wa = tc::su32(wst + s * kWBox), xa = tc::su32(xsplit + kb * kXBlock);
 #pragma unroll
                         for (int kk = 0; kk < kKB / 32; ++kk)
-                            mma_f8(d, sw128_desc(wa + kk * 32), sw128_desc(xa + kk * 32), (kb > 0 || kk > 0) ? 1u : 0u);
-                        commit(empty0 + 8 * s);
+                            tc::mma_f8(d, tc::sw128_desc(wa + kk * 32), tc::sw128_desc(xa + kk * 32), kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        tc::commit(empty0 + 8 * s);
                     }
-                    commit(accf0 + 8 * b);
+                    tc::commit(accf0 + 8 * b);
                 }
             }
         } else {
@@ -311,20 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jt = 0; jt < my_tiles; ++jt) {
                 const int b = jt & 1;
                 const uint32_t use = static_cast<uint32_t>(jt >> 1);
-                if (!wait(accf0 + 8 * b, use & 1u, abort_flag)) break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                if (!tc::bar_wait(accf0 + 8 * b, use & 1u, abort_flag)) break;
+                tc::fence_after();
                 uint32_t v[16];
-                asm volatile(
-                    "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-                    "%12, %13, %14, %15}, [%16];"
-                    : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-                      "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-                      "=r"(v[14]), "=r"(v[15])
-                    : "r"(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * kBRows)));
-                asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * kBRows), v);
+                tc::fence_before();
                 __syncwarp();
-                if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(acce0 + 8 * b) : "memory");
+                if (lane == 0) tc::bar_arrive(acce0 + 8 * b);
                 const int n = (blockIdx.x + jt * G) * kRows + row;
                 if (n < a.N) {
 #pragma unroll

@@ -84,7 +84,7 @@ typedef enum {
  *   DG_VAR_CC_WARP: [0] rows per warp R (1, 2, 4, 8), [1] warps per CTA (2..16),
  *                   [2] CTAs per SM cap (0 = occupancy limit)
  *   DG_VAR_CC_BULK: [0] 0, [1] pipeline stages (0 = as many as fit), [2] CTAs per SM (0 = 1)
- *   DG_VAR_TC:      [0] pipeline stages, [1] K-splits (0 = derived from the shape)
+ *   DG_VAR_TC:      [0] pipeline stages (0 = derived from the shape)
  * For the MoE ops, params[3] is the N-tile width in rows (0 = derived) and
  * params[4] the most (token, slot) pairs of one expert per pass over its rows
  * (1, 2, 4 or 8; 0 = 2). */

@@ -129,19 +129,20 @@ def test_calls_do_not_synchronise(cuda_device):
     M, N, K = 4, 1024, 1024
     x, W = S.linear_inputs(M, N, K, device=cuda_device)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_device)
-    ws = dg.workspace(dg.DG_OP_HEAD_FP8_ARGMAX, M, 8192, K)
+    ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K)
+    ws_h = dg.workspace(dg.DG_OP_HEAD_FP8_ARGMAX, M, 8192, K)
     _, Wq, scale = S.head_inputs(M, 8192, K, device=cuda_device)
     lg = torch.empty((M, 8192), dtype=torch.bfloat16, device=cuda_device)
     am = torch.empty((M,), dtype=torch.int32, device=cuda_device)
     dg.dg_gemv_bf16(x, W, y=y, ws=ws)
-    dg.dg_head_fp8_argmax(x, Wq, scale, logits=lg, argmax=am, ws=ws)
+    dg.dg_head_fp8_argmax(x, Wq, scale, logits=lg, argmax=am, ws=ws_h)
     torch.cuda.synchronize()
     prev = torch.cuda.get_sync_debug_mode()
     torch.cuda.set_sync_debug_mode("error")
     try:
         for _ in range(3):
             dg.dg_gemv_bf16(x, W, y=y, ws=ws)
-            dg.dg_head_fp8_argmax(x, Wq, scale, logits=lg, argmax=am, ws=ws)
+            dg.dg_head_fp8_argmax(x, Wq, scale, logits=lg, argmax=am, ws=ws_h)
     finally:
         torch.cuda.set_sync_debug_mode(prev)
     torch.cuda.synchronize()
