@@ -102,17 +102,37 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
             out->variant = DG_VAR_TC;      // dense enough for the tensor cores
             break;
         }
-        // Enough 8-warp CTAs to put two on every SM of a 152-SM part.
-        // Rows per warp / warps per CTA as measured on GB300 (dg_sweep): one row per
-        // warp at M = 1, more rows per warp as M grows (x reuse), small CTAs.
+        // Rows per warp [0], warps per CTA [1] and K-split warps [3] as dg_sweep
+        // measured them on GB300 for one and two tokens: long rows with few row groups
+        // share each group's K segments between warps; many short rows do not.
         const long rows = op == DG_OP_GATE_UP_SILU ? 2L * N : static_cast<long>(N);
-        if (M <= 1)
-            out->params[0] = op == DG_OP_GATE_UP_SILU ? 2 : (rows >= 8192 && rows < 16384 ? 2 : 1);
-        else if (M <= 2)
-            out->params[0] = rows >= 8192 ? 4 : 2;
-        else
-            out->params[0] = rows >= 8192 ? 4 : 2;
-        out->params[1] = 4;
+        const int nseg = (K + kSeg - 1) / kSeg;
+        int R, wpc, ks;
+        if (op == DG_OP_GATE_UP_SILU) {
+            R = 2;
+            wpc = M <= 1 ? 4 : 8;
+            ks = M <= 1 ? 4 : 1;
+        } else if (rows >= 32768) {
+            R = M <= 1 ? 1 : 2;
+            wpc = 8;
+            ks = 1;
+        } else if (rows >= 12288) {
+            R = 4;
+            wpc = 4;
+            ks = M <= 1 ? 4 : 2;
+        } else if (rows >= 8192) {
+            R = 2;
+            wpc = M <= 1 ? 4 : 8;
+            ks = 1;
+        } else {
+            R = (M <= 1 && K <= 4096) ? 2 : 4;
+            wpc = 8;
+            ks = 2;
+        }
+        while (ks > 1 && nseg < ks) ks /= 2;          // no warp without a segment
+        out->params[0] = R;
+        out->params[1] = wpc;
+        out->params[3] = ks > 1 ? ks : 0;
         break;
     }
     case DG_OP_HEAD_FP8_ARGMAX:
@@ -347,8 +367,10 @@ dg_status launch_dense(dg_op op, const DeviceInfo* dev, const dg_choice& c, Dens
     int R = c.params[0] > 0 ? c.params[0] : 4;
     const int wpc = c.params[1] > 0 ? c.params[1] : 8;
     const int cap = c.params[2];
+    const int ks = c.params[3] > 0 ? c.params[3] : 1;
     if ((R != 1 && R != 2 && R != 4 && R != 8) || wpc < 1 || wpc > 8 || cap < 0)
         return DG_ERR_BAD_VARIANT;
+    if ((ks != 1 && ks != 2 && ks != 4 && ks != 8) || wpc % ks != 0) return DG_ERR_BAD_VARIANT;
     if (op == DG_OP_GATE_UP_SILU && R < 2) return DG_ERR_BAD_VARIANT;
     int mt_max = static_cast<int>(kXsBudget / (static_cast<size_t>(a.K) * 2));
     if (mt_max > 8) mt_max = 8;
@@ -359,19 +381,25 @@ dg_status launch_dense(dg_op op, const DeviceInfo* dev, const dg_choice& c, Dens
         int r = R;
         while (r > 1 && r * cpow2(mt) > 32) r >>= 1;       // same arithmetic, fewer rows per warp
         if (op == DG_OP_GATE_UP_SILU && r < 2) return DG_ERR_UNSUPPORTED_SHAPE;
-        const void* fn = op == DG_OP_GEMV_BF16      ? dense_kernel_gemv(mt, r)
-                         : op == DG_OP_GATE_UP_SILU ? dense_kernel_gateup(mt, r)
-                                                    : dense_kernel_head(mt, r);
+        const int kse = mt <= 2 ? ks : 1;                 // K-split kernels exist for 1-2 token chunks
+        const void* fn = op == DG_OP_GEMV_BF16      ? dense_kernel_gemv(mt, r, kse > 1)
+                         : op == DG_OP_GATE_UP_SILU ? dense_kernel_gateup(mt, r, kse > 1)
+                                                    : dense_kernel_head(mt, r, kse > 1);
         if (!fn) return DG_ERR_BAD_VARIANT;
         const int threads = wpc * 32;
-        const size_t smem = static_cast<size_t>(mt) * a.K * 2;
+        const int slots = wpc / kse;                      // row groups per CTA round
+        size_t smem = static_cast<size_t>(mt) * a.K * 2;
+        if (kse > 1)                                      // segment partials of the K-split
+            smem += static_cast<size_t>(slots) * ((a.K + kSeg - 1) / kSeg) * r * cpow2(mt) * 4;
+        if (smem > kMaxDynSmem) return DG_ERR_UNSUPPORTED_SHAPE;
         int occ = occupancy(fn, threads, smem);
         if (occ < 1) return DG_ERR_UNSUPPORTED_SHAPE;
         if (cap > 0 && occ > cap) occ = cap;
         DenseArgs la = a;
         la.t0 = t0;
         la.groups = (a.N + r - 1) / r;
-        long long need = (la.groups + wpc - 1) / wpc;
+        la.ksplit = kse;
+        long long need = (la.groups + slots - 1) / slots;
         long long grid = static_cast<long long>(dev->sm_count) * occ;
         if (grid > need) grid = need;
         if (grid > kMaxGrid) grid = kMaxGrid;

@@ -24,6 +24,7 @@ struct DenseArgs {
     int K;
     int t0;                 // first token of this launch's chunk
     int groups;             // ceil(N / R)
+    int ksplit;             // KSPLIT kernels: warps sharing one row group's segments (2, 4 or 8; divides wpc)
     uint16_t* out;          // bf16 output: y [M, N], gate/up out [M, N/2], or head logits (may be null)
     int ld_out;             // output row stride in elements
     const float* scale;     // head: per-tensor scale (device)
@@ -122,6 +123,28 @@ __device__ __forceinline__ void load_segment(uint4 (&w)[kSeg / (32 * WTraits<WT>
     }
 }
 
+// Canonical-order partial of segment s (lane chains, then the butterfly): lanes
+// with idx = lane >> SH return the partial of output idx.
+template <int WT, int MT, int R>
+__device__ __forceinline__ float segment_partial(const uint4 (&w)[kSeg / (32 * WTraits<WT>::VE)][R], int K, int s,
+                                                 const uint4* xs_smem, int xstride, int lane)
+{
+    constexpr int VE = WTraits<WT>::VE;
+    constexpr int VPS = kSeg / (32 * VE);
+    constexpr int MTP = cpow2(MT);
+    constexpr int Q = R * MTP;
+    float p[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) p[q] = 0.0f;
+#pragma unroll
+    for (int v = 0; v < VPS; ++v) {
+        const int k = s * kSeg + v * (32 * VE) + lane * VE;
+        if (k < K) fma_vector<WT, MT, R, MTP>(w[v], xs_smem + k / 8, xstride, p);
+    }
+    reduce_scatter<Q>(p, lane);
+    return p[0];
+}
+
 // Canonical-order partial of segment s (lane chains, then the butterfly), folded
 // into `total`.
 template <int WT, int MT, int R>
@@ -164,7 +187,7 @@ __device__ __forceinline__ float row_group_total(const uint8_t* const (&wrow)[R]
     return total;
 }
 
-template <int WT, int MT, int R, int EPI>
+template <int WT, int MT, int R, int EPI, bool KSPLIT>
 __global__ void __launch_bounds__(256) cc_dense_kernel(DenseArgs a)
 {
     constexpr int MTP = cpow2(MT);
@@ -208,16 +231,8 @@ __global__ void __launch_bounds__(256) cc_dense_kernel(DenseArgs a)
     float scale = 1.0f;
     if constexpr (EPI == EPI_HEAD) scale = *a.scale;
 
-    for (int g = blockIdx.x * wpc + warp; g < a.groups; g += gridDim.x * wpc) {
-        const int row0 = g * R;
-        const uint8_t* wrow[R];
-        bool rok[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            rok[r] = (row0 + r) < a.N;
-            wrow[r] = a.W + static_cast<size_t>(rok[r] ? row0 + r : 0) * a.K * WTraits<WT>::ESZ;
-        }
-        const float total = row_group_total<WT, MT, R>(wrow, rok, a.K, xs, kv, lane);
+    // Per row group: `total` -> the op's output (and the head's running pick).
+    auto emit = [&](int row0, float total) {
         const int row = row0 + my_r;
         if constexpr (EPI == EPI_STORE) {
             if (writer && row < a.N)
@@ -241,6 +256,60 @@ __global__ void __launch_bounds__(256) cc_dense_kernel(DenseArgs a)
                     best_i = row;
                 }
             }
+        }
+    };
+
+    if constexpr (!KSPLIT) {
+        for (int g = blockIdx.x * wpc + warp; g < a.groups; g += gridDim.x * wpc) {
+            const int row0 = g * R;
+            const uint8_t* wrow[R];
+            bool rok[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                rok[r] = (row0 + r) < a.N;
+                wrow[r] = a.W + static_cast<size_t>(rok[r] ? row0 + r : 0) * a.K * WTraits<WT>::ESZ;
+            }
+            emit(row0, row_group_total<WT, MT, R>(wrow, rok, a.K, xs, kv, lane));
+        }
+    } else {
+        // K-split inside the CTA: the ksplit warps of a slot share one row group,
+        // warp `part` taking segments part, part + ksplit, ...; the segment partials
+        // meet in shared memory and are folded left in segment order by the slot's
+        // first warp -- the same sums in the same order as one warp doing them all.
+        constexpr int VPS = kSeg / (32 * WTraits<WT>::VE);
+        const int ks = a.ksplit, slots = wpc / ks;
+        const int slot = warp / ks, part = warp - slot * ks;
+        const int nseg = (a.K + kSeg - 1) / kSeg;
+        float* P = reinterpret_cast<float*>(xs + MT * kv) + static_cast<size_t>(slot) * nseg * Q;
+        const int idx_w = lane >> SH;
+        const bool idx_writer = (lane & ((1 << SH) - 1)) == 0;
+        const int per_round = gridDim.x * slots;
+        const int rounds = (a.groups + per_round - 1) / per_round;
+        for (int rd = 0; rd < rounds; ++rd) {
+            const int g = rd * per_round + blockIdx.x * slots + slot;
+            const int row0 = g * R;
+            if (g < a.groups) {
+                const uint8_t* wrow[R];
+                bool rok[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    rok[r] = (row0 + r) < a.N;
+                    wrow[r] = a.W + static_cast<size_t>(rok[r] ? row0 + r : 0) * a.K * WTraits<WT>::ESZ;
+                }
+                for (int s = part; s < nseg; s += ks) {
+                    uint4 w[VPS][R];
+                    load_segment<WT, R>(w, wrow, rok, a.K, s, lane);
+                    const float ps = segment_partial<WT, MT, R>(w, a.K, s, xs, kv, lane);
+                    if (idx_writer) P[s * Q + idx_w] = ps;
+                }
+            }
+            __syncthreads();
+            if (part == 0 && g < a.groups) {
+                float total = P[idx_w];
+                for (int s = 1; s < nseg; ++s) total = total + P[s * Q + idx_w];
+                emit(row0, total);
+            }
+            __syncthreads();
         }
     }
 

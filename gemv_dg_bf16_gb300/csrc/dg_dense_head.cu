@@ -3,6 +3,6 @@
 #include "dg_dense_table.cuh"
 
 namespace dg {
-const void* dense_kernel_head(int mt, int R) { return dense_lookup<WT_E4M3, EPI_HEAD>(mt, R); }
+const void* dense_kernel_head(int mt, int R, bool ksplit) { return dense_lookup<WT_E4M3, EPI_HEAD>(mt, R, ksplit); }
 const void* bulk_kernel_head(int mt) { return bulk_lookup<WT_E4M3, EPI_HEAD>(mt); }
 }  // namespace dg

@@ -15,38 +15,42 @@ constexpr bool dense_valid()
 }
 
 template <int WT, int EPI, int MT, int R>
-const void* dense_one()
+const void* dense_one(bool ksplit)
 {
-    if constexpr (dense_valid<WT, EPI, MT, R>())
-        return reinterpret_cast<const void*>(&cc_dense_kernel<WT, MT, R, EPI>);
-    else
+    if constexpr (dense_valid<WT, EPI, MT, R>()) {
+        // The in-CTA K-split is built for the few-token chunks that use it.
+        if constexpr (MT <= 2)
+            if (ksplit) return reinterpret_cast<const void*>(&cc_dense_kernel<WT, MT, R, EPI, true>);
+        return ksplit ? nullptr : reinterpret_cast<const void*>(&cc_dense_kernel<WT, MT, R, EPI, false>);
+    } else {
         return nullptr;
+    }
 }
 
 template <int WT, int EPI, int MT>
-const void* dense_by_r(int R)
+const void* dense_by_r(int R, bool ksplit)
 {
     switch (R) {
-    case 1: return dense_one<WT, EPI, MT, 1>();
-    case 2: return dense_one<WT, EPI, MT, 2>();
-    case 4: return dense_one<WT, EPI, MT, 4>();
-    case 8: return dense_one<WT, EPI, MT, 8>();
+    case 1: return dense_one<WT, EPI, MT, 1>(ksplit);
+    case 2: return dense_one<WT, EPI, MT, 2>(ksplit);
+    case 4: return dense_one<WT, EPI, MT, 4>(ksplit);
+    case 8: return dense_one<WT, EPI, MT, 8>(ksplit);
     default: return nullptr;
     }
 }
 
 template <int WT, int EPI>
-const void* dense_lookup(int mt, int R)
+const void* dense_lookup(int mt, int R, bool ksplit)
 {
     switch (mt) {
-    case 1: return dense_by_r<WT, EPI, 1>(R);
-    case 2: return dense_by_r<WT, EPI, 2>(R);
-    case 3: return dense_by_r<WT, EPI, 3>(R);
-    case 4: return dense_by_r<WT, EPI, 4>(R);
-    case 5: return dense_by_r<WT, EPI, 5>(R);
-    case 6: return dense_by_r<WT, EPI, 6>(R);
-    case 7: return dense_by_r<WT, EPI, 7>(R);
-    case 8: return dense_by_r<WT, EPI, 8>(R);
+    case 1: return dense_by_r<WT, EPI, 1>(R, ksplit);
+    case 2: return dense_by_r<WT, EPI, 2>(R, ksplit);
+    case 3: return dense_by_r<WT, EPI, 3>(R, ksplit);
+    case 4: return dense_by_r<WT, EPI, 4>(R, ksplit);
+    case 5: return dense_by_r<WT, EPI, 5>(R, ksplit);
+    case 6: return dense_by_r<WT, EPI, 6>(R, ksplit);
+    case 7: return dense_by_r<WT, EPI, 7>(R, ksplit);
+    case 8: return dense_by_r<WT, EPI, 8>(R, ksplit);
     default: return nullptr;
     }
 }

@@ -11,9 +11,9 @@ namespace dg {
 
 // Kernel entry points of the dense CUDA-core family, by (op, tokens in the
 // launch's chunk, rows per warp).  nullptr when that combination is not built.
-const void* dense_kernel_gemv(int mt, int R);
-const void* dense_kernel_gateup(int mt, int R);
-const void* dense_kernel_head(int mt, int R);
+const void* dense_kernel_gemv(int mt, int R, bool ksplit);
+const void* dense_kernel_gateup(int mt, int R, bool ksplit);
+const void* dense_kernel_head(int mt, int R, bool ksplit);
 // Bulk-staged variant of the same family (dg_cc_bulk.cuh), by tokens in the chunk.
 const void* bulk_kernel_gemv(int mt);
 const void* bulk_kernel_gateup(int mt);

@@ -211,8 +211,12 @@ std::string check_choice(int op, const dg_choice& c)
     if (wpc < 1 || wpc > 8) return "warps per CTA must be 1..8";
     for (int i = 2; i < 6; ++i)
         if (c.params[i] < 0) return "negative parameter";
-    if (op != DG_OP_MOE_W1 && op != DG_OP_MOE_W2 && (c.params[3] != 0 || c.params[4] != 0))
-        return "unused parameter set";
+    if (op != DG_OP_MOE_W1 && op != DG_OP_MOE_W2) {
+        const int ks = c.params[3];
+        if (ks != 0 && ks != 1 && ks != 2 && ks != 4 && ks != 8) return "K-split warps must be 1, 2, 4 or 8";
+        if (ks > 1 && wpc % ks != 0) return "K-split warps must divide warps per CTA";
+        if (c.params[4] != 0) return "unused parameter set";
+    }
     return "";
 }
 

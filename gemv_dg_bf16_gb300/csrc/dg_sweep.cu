@@ -118,10 +118,11 @@ std::vector<dg_choice> candidates(int op, const dg_choice& def)
                 }
     } else {
         for (int R : {1, 2, 4, 8})
-            for (int wpc : {4, 8}) {
-                if (op == DG_OP_GATE_UP_SILU && R < 2) continue;
-                add(mk(DG_VAR_CC_WARP, R, wpc, 0));
-            }
+            for (int wpc : {4, 8})
+                for (int ks : {1, 2, 4}) {
+                    if (op == DG_OP_GATE_UP_SILU && R < 2) continue;
+                    add(mk(DG_VAR_CC_WARP, R, wpc, 0, ks > 1 ? ks : 0));
+                }
         for (int cps : {1, 2})
             for (int st : {0, 4, 8}) add(mk(DG_VAR_CC_BULK, 0, st, cps));
     }

@@ -81,8 +81,10 @@ typedef enum {
 } dg_variant;
 
 /* params[] meaning by variant:
- *   DG_VAR_CC_WARP: [0] rows per warp R (1, 2, 4, 8), [1] warps per CTA (2..16),
- *                   [2] CTAs per SM cap (0 = occupancy limit)
+ *   DG_VAR_CC_WARP: [0] rows per warp R (1, 2, 4, 8), [1] warps per CTA (1..8),
+ *                   [2] CTAs per SM cap (0 = occupancy limit), [3] dense ops: warps
+ *                   sharing one row group's K segments (1, 2, 4, 8 dividing [1];
+ *                   0 = 1) -- the segment partials are folded in the same order
  *   DG_VAR_CC_BULK: [0] 0, [1] pipeline stages (0 = as many as fit), [2] CTAs per SM (0 = 1)
  *   DG_VAR_TC:      [0] pipeline stages (0 = derived from the shape)
  * For the MoE ops, params[3] is the N-tile width in rows (0 = derived) and

@@ -56,19 +56,22 @@ def test_gemv_sweep_full_size_sampled(cuda_device, M, N, K):
 
 
 def _variants(op, mt_max):
-    """Every CUDA-core variant: register-streamed (rows/warp, warps/CTA, CTA cap) and
-    bulk-staged (pipeline depth, CTAs per SM).  All share one arithmetic."""
+    """Every CUDA-core variant: register-streamed (rows/warp, warps/CTA, CTA cap, warps
+    sharing a row group's K segments) and bulk-staged (pipeline depth, CTAs per SM).
+    All share one arithmetic."""
     out = []
     for R, wpc, cap in itertools.product((1, 2, 4, 8), (2, 4, 8), (0, 1)):
         if op == dg.DG_OP_GATE_UP_SILU and R < 2:
             continue
-        out.append(dg.Choice.make(dg.DG_VAR_CC_WARP, R, wpc, cap))
+        for ks in sorted({1, 2, wpc}):
+            out.append(dg.Choice.make(dg.DG_VAR_CC_WARP, R, wpc, cap, ks if ks > 1 else 0))
     for st, cps in itertools.product((0, 2, 3, 8), (1, 2)):
         out.append(dg.Choice.make(dg.DG_VAR_CC_BULK, 0, st, cps))
     return out
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1000, 3080), (3, 515, 1024), (8, 256, 4096), (13, 70, 2048)])
+@pytest.mark.parametrize("M,N,K", [(1, 1000, 3080), (2, 300, 8200), (1, 77, 520), (3, 515, 1024), (8, 256, 4096),
+                                   (13, 70, 2048)])
 def test_gemv_cc_variants_bitwise_identical(cuda_device, M, N, K):
     x, W = S.linear_inputs(M, N, K, device=cuda_device)
     ref = dg.dg_gemv_bf16(x, W, choice=CC)
@@ -161,8 +164,9 @@ def test_gate_up_full_size_sampled(cuda_device, M):
     _gate_up_check(x, Wgu, out, cols=sample_rows(12288, 64, seed=M))
 
 
-def test_gate_up_variants_bitwise_identical(cuda_device):
-    x, Wgu = S.gate_up_inputs(6, 300, 2056, device=cuda_device)
+@pytest.mark.parametrize("M,K", [(1, 5128), (2, 3080), (6, 2056)])
+def test_gate_up_variants_bitwise_identical(cuda_device, M, K):
+    x, Wgu = S.gate_up_inputs(M, 300, K, device=cuda_device)
     ref = dg.dg_gate_up_silu(x, Wgu, choice=CC)
     for c in _variants(dg.DG_OP_GATE_UP_SILU, 8):
         try:

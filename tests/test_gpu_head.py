@@ -98,11 +98,12 @@ def test_head_tc_activations_with_wide_dynamic_range(cuda_device):
     _check_argmax(x, Wq, scale, am)
 
 
-def test_head_variants_bitwise_identical(cuda_device):
-    x, Wq, scale = S.head_inputs(5, 3001, 2064, device=cuda_device)
+@pytest.mark.parametrize("M", [1, 5])
+def test_head_variants_bitwise_identical(cuda_device, M):
+    x, Wq, scale = S.head_inputs(M, 3001, 2064, device=cuda_device)
     ref_l, ref_a = dg.dg_head_fp8_argmax(x, Wq, scale, choice=FAMILIES["cc"])
-    choices = [dg.Choice.make(dg.DG_VAR_CC_WARP, R, wpc, cap)
-               for R in (1, 2, 4, 8) for wpc in (2, 4, 8) for cap in (0, 1)]
+    choices = [dg.Choice.make(dg.DG_VAR_CC_WARP, R, wpc, cap, ks)
+               for R in (1, 2, 4, 8) for wpc in (2, 4, 8) for cap in (0, 1) for ks in (0, 2)]
     choices += [dg.Choice.make(dg.DG_VAR_CC_BULK, 0, st, cps) for st in (0, 2, 5, 16) for cps in (1, 2)]
     for c in choices:
         try:

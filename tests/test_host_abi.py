@@ -147,6 +147,10 @@ def test_table_valid(tmp_path):
      "even"),
     (dict(entries=[{"op": "nope", "M": 4, "N": 1, "K": 8, "pick": {"variant": 1, "params": [4, 8]}}]),
      "unknown op"),
+    (dict(entries=[{"op": "gemv_bf16", "M": 1, "N": 1, "K": 8, "pick": {"variant": 1, "params": [4, 4, 0, 3]}}]),
+     "K-split warps must be 1, 2, 4 or 8"),
+    (dict(entries=[{"op": "gemv_bf16", "M": 1, "N": 1, "K": 8, "pick": {"variant": 1, "params": [4, 2, 0, 4]}}]),
+     "divide warps per CTA"),
     (dict(entries=[{"op": "gemv_bf16", "M": 4, "N": 1, "K": 8}]), "pick"),
     (dict(format="other"), "not a libdecodegemm table"),
 ])
