@@ -39,11 +39,16 @@ constexpr int kKB = 64;                           // K per stage: one 128-byte s
 constexpr int kWBox = kTileRows * kKB * 2;        // 16 KB
 constexpr int kThreads = 192;
 constexpr int kMaxCluster = 8;                    // portable thread-block cluster size
+constexpr size_t kCoResidentSmem = 112 * 1024;    // two CTAs per SM
+constexpr int kPushMaxTokens = 8;                 // push fold up to this many tokens
 
 struct TcArgs {
     int N, K, M;
     int nsplit, nkb, tiles;
     int stages;
+    int push;             // clustered: ranks push their rows into the owners' shared memory
+    int mq;               // tokens pushed per row (M rounded up to 4)
+    int slice_max;        // most rows one rank folds
     uint16_t* out;
     int ld_out;
     uint8_t* ws;          // status word only (the K-split fold stays on chip)
@@ -68,6 +73,18 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t ra
     uint32_t r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
     return r;
+}
+
+// Rows [lo, hi) of a 128-row tile folded by rank r of an ns-rank cluster
+// (multiples of 4, so a (gate, up) row pair never straddles two ranks).
+__host__ __device__ inline int slice_lo(int r, int ns) { return (r * (kTileRows / 4) / ns) * 4; }
+
+// Four fp32 into a peer's shared memory; the bytes count on the peer's mbarrier.
+__device__ __forceinline__ void st_async_f32x4(uint32_t remote, float a, float b, float c, float d, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(remote), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+                 : "memory");
 }
 
 // Four consecutive fp32 from a cluster peer's shared memory (read after a cluster
@@ -132,9 +149,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = a.stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kStage);   // full[S], empty[S], accum
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kStage);   // full[S], empty[S], accum, recv
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+    // Push fold: rows pushed here by every rank, [rank][slice row][mq] fp32.
+    float* recv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + (2 * S + 2) * 8 + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool clustered = a.nsplit > 1;
@@ -145,7 +164,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nkb = kb1 - kb0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2 * S + 1; ++s) tc::bar_init(tc::su32(bars + s), 1);
+        for (int s = 0; s < 2 * S + 2; ++s) tc::bar_init(tc::su32(bars + s), 1);
+        if (clustered && a.push) {
+            // every rank pushes this rank's slice of rows, mq tokens each
+            const int rows = slice_lo(split + 1, a.nsplit) - slice_lo(split, a.nsplit);
+            tc::bar_expect_tx(tc::su32(bars + 2 * S + 1), static_cast<uint32_t>(a.nsplit * rows * a.mq * 4));
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -161,6 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_holder;
     const uint32_t full0 = tc::su32(bars), empty0 = tc::su32(bars + S), accum = tc::su32(bars + 2 * S);
+    const uint32_t recv_bar = tc::su32(bars + 2 * S + 1);
 
     pdl_launch_dependents();
     if (warp == 0) {
@@ -229,6 +254,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                     emit<EPI>(a, t, n, __uint_as_float(v[j]), t < a.M && n < a.N);
                 }
             }
+        } else if (a.push) {
+            // Push row `row` of this rank's partial tile (tokens 0..mq-1) into the
+            // shared memory of the rank that folds it.
+            int owner = 0;
+            while (owner + 1 < a.nsplit && row >= slice_lo(owner + 1, a.nsplit)) ++owner;
+            const uint32_t dst = map_to_rank(tc::su32(recv), static_cast<uint32_t>(owner)) +
+                                 static_cast<uint32_t>(((split * a.slice_max + row - slice_lo(owner, a.nsplit)) * a.mq) * 4);
+            const uint32_t dbar = map_to_rank(recv_bar, static_cast<uint32_t>(owner));
+#pragma unroll 1
+            for (int c = 0; c < MP / 16 && c * 16 < a.mq; ++c) {
+                uint32_t v[16];
+                tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
+#pragma unroll
+                for (int j = 0; j < 16; j += 4)
+                    if (c * 16 + j < a.mq)
+                        st_async_f32x4(dst + (c * 16 + j) * 4, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                       __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), dbar);
+            }
+            // This rank's slice: wait for every rank's rows, fold them in rank order.
+            const int lo = slice_lo(split, a.nsplit), hi = slice_lo(split + 1, a.nsplit);
+            const bool got = tc::bar_wait(recv_bar, 0, abort_flag);
+            if (got) {
+                const int r = threadIdx.x - 64;            // 0..127: one folded row per thread
+                const bool mine = r < hi - lo;
+                const int nr = tile * kTileRows + lo + r;
+#pragma unroll 1
+                for (int t = 0; t < a.mq; t += 4) {
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (mine) {
+                        acc = *reinterpret_cast<const float4*>(recv + (static_cast<size_t>(r) * a.mq + t));
+                        for (int s2 = 1; s2 < a.nsplit; ++s2) {
+                            const float4 v = *reinterpret_cast<const float4*>(
+                                recv + ((static_cast<size_t>(s2) * a.slice_max + r) * a.mq + t));
+                            acc.x = acc.x + v.x;
+                            acc.y = acc.y + v.y;
+                            acc.z = acc.z + v.z;
+                            acc.w = acc.w + v.w;
+                        }
+                    }
+                    emit<EPI>(a, t + 0, nr, acc.x, mine && t + 0 < a.M && nr < a.N);
+                    emit<EPI>(a, t + 1, nr, acc.y, mine && t + 1 < a.M && nr < a.N);
+                    emit<EPI>(a, t + 2, nr, acc.z, mine && t + 2 < a.M && nr < a.N);
+                    emit<EPI>(a, t + 3, nr, acc.w, mine && t + 3 < a.M && nr < a.N);
+                }
+            } else if (row == 0) {
+                set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
+            }
         } else {
             // Park this rank's partial tile P[t][row] (fp32) in the now idle stage memory.
             float* P = reinterpret_cast<float*>(smem);
@@ -242,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     }
-    if (clustered) {
+    if (clustered && !a.push) {
         cluster_sync_all();                  // every rank's partial tile is in place
         if (warp >= 2) {
             // This rank folds rows [lo, hi) (multiples of 4) for all tokens: P_0 + P_1 + ...
@@ -271,17 +343,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t off = static_cast<uint32_t>((tt[u] * kTileRows + rr[u]) * 4);
                         acc[u] = vv[u] ? ld_dsmem_f32x4(peer[0] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
+                    // every rank's loads first (they overlap), then the adds in rank order
+                    float4 pv[kMaxCluster - 1][2];
+#pragma unroll
+                    for (int s2 = 1; s2 < kMaxCluster; ++s2)
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            pv[s2 - 1][u] = (s2 < a.nsplit && vv[u])
+                                ? ld_dsmem_f32x4(peer[s2] + static_cast<uint32_t>((tt[u] * kTileRows + rr[u]) * 4))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int s2 = 1; s2 < kMaxCluster; ++s2) {
                         if (s2 >= a.nsplit) break;
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            if (!vv[u]) continue;
-                            const float4 v = ld_dsmem_f32x4(peer[s2] + static_cast<uint32_t>((tt[u] * kTileRows + rr[u]) * 4));
-                            acc[u].x = acc[u].x + v.x;
-                            acc[u].y = acc[u].y + v.y;
-                            acc[u].z = acc[u].z + v.z;
-                            acc[u].w = acc[u].w + v.w;
+                            acc[u].x = acc[u].x + pv[s2 - 1][u].x;
+                            acc[u].y = acc[u].y + pv[s2 - 1][u].y;
+                            acc[u].z = acc[u].z + pv[s2 - 1][u].z;
+                            acc[u].w = acc[u].w + pv[s2 - 1][u].w;
                         }
                     }
 #pragma unroll
@@ -348,10 +427,26 @@ const void* tc_lookup(int mp, int epi)
     }
 }
 
-int default_stages(int mp)
+size_t stage_bytes(int mp) { return kWBox + static_cast<size_t>(mp) * kKB * 2; }
+
+// Bytes of the push fold's receive buffer (0 when the tile is not split).
+int slice_max(int ns) { return ((kTileRows / 4 + ns - 1) / ns) * 4; }
+
+size_t recv_bytes(int ns, int mq) { return ns > 1 ? static_cast<size_t>(ns) * slice_max(ns) * mq * 4 : 0; }
+
+size_t smem_bytes(int mp, int stages, size_t recv)
 {
-    // Two CTAs per SM: about 100 KB of shared memory each.
-    return mp <= 32 ? 5 : (mp <= 64 ? 4 : 3);
+    return 1024 + stages * stage_bytes(mp) + (2 * stages + 2) * 8 + 16 + recv;
+}
+
+// Two CTAs per SM (about 113 KB each) let the next launch's prologue and first
+// weight boxes overlap this launch's tail: as many stages as fit that budget
+// beside the receive buffer, at most 5.
+int default_stages(int mp, size_t recv)
+{
+    int s = 5;
+    while (s > 2 && smem_bytes(mp, s, recv) > kCoResidentSmem) --s;
+    return s;
 }
 
 }  // namespace
@@ -388,10 +483,17 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
     const int epi = gate_up ? 1 : 0;
     const void* fn = tc_lookup(mp, epi);
     if (!fn) return DG_ERR_BAD_VARIANT;
-    int stages = c.params[0] > 0 ? c.params[0] : default_stages(mp);
+    const int ns = tc_nsplit(N, K, M);
+    const int mq = (M + 3) & ~3;
+    // K-split fold: ranks push their rows to the folding rank (st.async) for up to 8
+    // tokens when the receive buffer costs no pipeline stage; otherwise each rank
+    // pulls the others' partials after a cluster barrier (measured on GB300: the
+    // push is faster for few tokens, equal or slower beyond).  Same bits either way.
+    size_t recv = mq <= kPushMaxTokens ? recv_bytes(ns, mq) : 0;
+    int stages = c.params[0] > 0 ? c.params[0] : default_stages(mp, 0);
     if (stages < 2 || stages > 8) return DG_ERR_BAD_VARIANT;
-    const size_t stage_bytes = kWBox + static_cast<size_t>(mp) * kKB * 2;
-    const size_t smem = 1024 + stages * stage_bytes + (2 * stages + 1) * 8 + 16;
+    if (recv > 0 && smem_bytes(mp, stages, recv) > (c.params[0] > 0 ? kMaxDynSmem : kCoResidentSmem)) recv = 0;
+    const size_t smem = smem_bytes(mp, stages, recv);
     if (smem > kMaxDynSmem) return DG_ERR_BAD_VARIANT;
     if (ws_bytes < tc_workspace_bytes(M, N, K)) return DG_ERR_WORKSPACE_TOO_SMALL;
     TcArgs a{};
@@ -400,9 +502,12 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
     a.M = M;
     a.tiles = (N + kTileRows - 1) / kTileRows;
     a.nkb = (K + kKB - 1) / kKB;
-    a.nsplit = tc_nsplit(N, K, M);
+    a.nsplit = ns;
+    a.push = recv > 0 ? 1 : 0;
+    a.mq = mq;
+    a.slice_max = slice_max(ns);
     const size_t part_bytes = static_cast<size_t>(mp) * kTileRows * 4;
-    if (a.nsplit > 1 && part_bytes > static_cast<size_t>(stages) * stage_bytes) return DG_ERR_BAD_VARIANT;
+    if (ns > 1 && !a.push && part_bytes > static_cast<size_t>(stages) * stage_bytes(mp)) return DG_ERR_BAD_VARIANT;
     a.stages = stages;
     a.out = static_cast<uint16_t*>(out);
     a.ld_out = ld_out;
