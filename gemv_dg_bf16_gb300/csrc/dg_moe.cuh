@@ -50,18 +50,21 @@ struct Route {
 };
 
 // Every CTA computes the same routing tables (deterministic, no atomics on order).
+// topk_ids is read from global memory once, into shared memory.
 __device__ inline void route_scan(Route& R, const int32_t* __restrict__ ids, int M, int topk, int E,
                            uint8_t* ws)
 {
+    __shared__ int sid[kMoeMaxPairs];
     const int P_all = M * topk;
+    for (int i = threadIdx.x; i < P_all; i += blockDim.x) sid[i] = ids[i];
     for (int e = threadIdx.x; e < E; e += blockDim.x) R.cnt[e] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < P_all; i += blockDim.x) {
         const int t = i / topk, k = i - t * topk;
-        const int e = ids[i];
+        const int e = sid[i];
         bool ok = e >= 0 && e < E;
         for (int j = 0; ok && j < k; ++j)
-            if (ids[t * topk + j] == e) ok = false;
+            if (sid[t * topk + j] == e) ok = false;
         R.valid[i] = ok ? 1 : 0;
         if (ok) atomicAdd(&R.cnt[e], 1);
         else if (blockIdx.x == 0) set_status(ws, DG_DEVERR_BAD_TOPK_ID);
@@ -105,10 +108,10 @@ __device__ inline void route_scan(Route& R, const int32_t* __restrict__ ids, int
     __syncthreads();
     for (int i = threadIdx.x; i < P_all; i += blockDim.x) {
         if (!R.valid[i]) continue;
-        const int e = ids[i];
+        const int e = sid[i];
         int rank = 0;
         for (int j = 0; j < i; ++j)
-            if (R.valid[j] && ids[j] == e) ++rank;
+            if (R.valid[j] && sid[j] == e) ++rank;
         const int pos = R.cnt[e] + rank;
         R.ptok[pos] = static_cast<int8_t>(i / topk);
         R.pslot[pos] = static_cast<int8_t>(i % topk);

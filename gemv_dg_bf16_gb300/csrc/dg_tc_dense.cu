@@ -16,10 +16,12 @@
 // contiguous ranges of 64-element blocks, a fixed function of (N, K, MP)
 // (tc_nsplit below); each range is one MMA chain from zero in ascending k; the
 // range partials are folded left in fp32.  The nsplit CTAs of a tile form one
-// thread-block cluster: each parks its fp32 partial tile in its own shared
-// memory, and after a cluster barrier each CTA folds a slice of the tile's rows
-// by reading every rank's partial through distributed shared memory, in rank
-// order.  Variants (pipeline depth) change no bits.
+// thread-block cluster and each rank folds a slice of the tile's rows, over all
+// ranks in rank order.  Up to 8 tokens the ranks push their rows into the folding
+// rank's shared memory (st.async, counted on its mbarrier); beyond that each rank
+// parks its partial tile in its own shared memory and, after a cluster barrier,
+// the folding ranks read them through distributed shared memory.  Pipeline depth
+// and the fold's transport change no bits.
 // Every mbarrier wait is bounded: on timeout the kernel flags
 // DG_DEVERR_WAIT_TIMEOUT in the workspace status word and winds down.
 #include <cuda.h>
