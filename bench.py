@@ -257,6 +257,8 @@ def run_gpu(args):
                  for r in routs], b2)
 
     n_cases = len(cases)
+    if n_cases == 0:
+        raise SystemExit(f"no benchmark case matches --cases {args.cases!r} / --only {args.only!r}")
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_cases)]
     times = [[] for _ in range(n_cases)]
 

@@ -132,7 +132,7 @@ template <bool W1, int MTMAX>
 __global__ void __launch_bounds__(256, MTMAX <= 2 ? 3 : 2) moe_kernel(MoeArgs a)
 {
     __shared__ Route R;
-    __shared__ int fold_flag;
+    __shared__ int8_t fold_tok[16];      // W2: pairs of the unit whose token this unit folds
     extern __shared__ uint4 xs[];        // [MTMAX][K/8]
     pdl_launch_dependents();
     pdl_wait();                          // routing and activations come from earlier kernels
@@ -172,33 +172,37 @@ __global__ void __launch_bounds__(256, MTMAX <= 2 ? 3 : 2) moe_kernel(MoeArgs a)
             run_chunk<W1, MTMAX>(c, a, R, e, lo, hi, p0, xs, terms);
         }
         if constexpr (!W1) {
-            // Publish this unit's terms, then take a ticket per token of the unit.
+            // Publish this unit's terms, then take every pair's (token, N-tile) ticket at
+            // once (one thread per pair; an expert's pairs are distinct tokens); the
+            // tokens whose last term this was are folded in slot order.
             __threadfence();
             __syncthreads();
-            for (int p = pb; p < pe; ++p) {
+            for (int p = pb + threadIdx.x; p < pe; p += blockDim.x) {
                 const int t = R.ptok[p];
-                if (threadIdx.x == 0) {
-                    const unsigned old = atomicAdd(&tickets[t * tiles + tile], 1u);
-                    fold_flag = (old + 1 == static_cast<unsigned>(R.nvalid[t]));
-                }
-                __syncthreads();
-                if (fold_flag) {
-                    __threadfence();
-                    for (int n = lo + threadIdx.x; n < hi; n += blockDim.x) {
-                        float y = 0.0f;
-                        bool first = true;
-                        for (int k = 0; k < a.topk; ++k) {
-                            if (!R.valid[t * a.topk + k]) continue;
-                            const float v = ld_cg_f32(terms + (static_cast<size_t>(t) * a.topk + k) * a.Nout + n);
-                            y = first ? v : y + v;
-                            first = false;
-                        }
-                        a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
-                    }
-                    if (threadIdx.x == 0) tickets[t * tiles + tile] = 0u;
-                }
-                __syncthreads();
+                const unsigned old = atomicAdd(&tickets[t * tiles + tile], 1u);
+                fold_tok[p - pb] = (old + 1 == static_cast<unsigned>(R.nvalid[t])) ? 1 : 0;
             }
+            __syncthreads();
+            bool any = false;
+            for (int p = pb; p < pe; ++p) {
+                if (!fold_tok[p - pb]) continue;
+                if (!any) __threadfence();
+                any = true;
+                const int t = R.ptok[p];
+                for (int n = lo + threadIdx.x; n < hi; n += blockDim.x) {
+                    float y = 0.0f;
+                    bool first = true;
+                    for (int k = 0; k < a.topk; ++k) {
+                        if (!R.valid[t * a.topk + k]) continue;
+                        const float v = ld_cg_f32(terms + (static_cast<size_t>(t) * a.topk + k) * a.Nout + n);
+                        y = first ? v : y + v;
+                        first = false;
+                    }
+                    a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
+                }
+                if (threadIdx.x == 0) tickets[t * tiles + tile] = 0u;
+            }
+            __syncthreads();                               // fold_tok reuse
         }
     }
 }

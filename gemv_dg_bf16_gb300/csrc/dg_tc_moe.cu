@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float red[4][kPairs];
     __shared__ float sig[kPairs], isig[kPairs];
     __shared__ float exch[kPairs][64];       // W1: up values of a tile's 64 columns
-    __shared__ int fold_flag;
+    __shared__ int8_t fold_tok[kPairs];   // W2: pairs of the pass whose token this pass folds
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
@@ -269,33 +269,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                             terms[(static_cast<size_t>(t) * a.topk + k) * a.Nout + n] = h * a.gw[t * a.topk + k];
                         }
                     }
-                    // Publish, then one ticket per (token, tile) for this chunk's pairs.
+                    // Publish, then take every pair's (token, tile) ticket at once (one
+                    // thread per pair; the pairs of a pass are distinct tokens); fold the
+                    // tokens whose last term this was, in slot order.
                     __threadfence();
                     asm volatile("bar.sync 1, 128;" ::: "memory");
-                    for (int p = 0; p < c; ++p) {
-                        const int t = R.ptok[p0 + p];
-                        if (et == 0) {
-                            const unsigned old = atomicAdd(&tickets[t * T + tile], 1u);
-                            fold_flag = (old + 1 == static_cast<unsigned>(R.nvalid[t]));
-                        }
-                        asm volatile("bar.sync 1, 128;" ::: "memory");
-                        if (fold_flag) {
-                            __threadfence();
-                            if (n < a.Nout) {
-                                float y = 0.0f;
-                                bool first = true;
-                                for (int k = 0; k < a.topk; ++k) {
-                                    if (!R.valid[t * a.topk + k]) continue;
-                                    const float tv = ld_cg_f32(terms + (static_cast<size_t>(t) * a.topk + k) * a.Nout + n);
-                                    y = first ? tv : y + tv;
-                                    first = false;
-                                }
-                                a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
-                            }
-                            if (et == 0) tickets[t * T + tile] = 0u;
-                        }
-                        asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (et < c) {
+                        const int t = R.ptok[p0 + et];
+                        const unsigned old = atomicAdd(&tickets[t * T + tile], 1u);
+                        fold_tok[et] = (old + 1 == static_cast<unsigned>(R.nvalid[t])) ? 1 : 0;
                     }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    bool any = false;
+                    for (int p = 0; p < c; ++p) {
+                        if (!fold_tok[p]) continue;
+                        if (!any) __threadfence();
+                        any = true;
+                        const int t = R.ptok[p0 + p];
+                        if (n < a.Nout) {
+                            float y = 0.0f;
+                            bool first = true;
+                            for (int k = 0; k < a.topk; ++k) {
+                                if (!R.valid[t * a.topk + k]) continue;
+                                const float tv = ld_cg_f32(terms + (static_cast<size_t>(t) * a.topk + k) * a.Nout + n);
+                                y = first ? tv : y + tv;
+                                first = false;
+                            }
+                            a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
+                        }
+                        if (et == 0) tickets[t * T + tile] = 0u;
+                    }
+                    asm volatile("bar.sync 1, 128;" ::: "memory");    // fold_tok reuse
                 }
             }
             return true;
