@@ -70,39 +70,52 @@ __device__ inline void route_scan(Route& R, const int32_t* __restrict__ ids, int
         else if (blockIdx.x == 0) set_status(ws, DG_DEVERR_BAD_TOPK_ID);
     }
     __syncthreads();
-    // Warp 0: exclusive scans over experts of (count > 0) and count.
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int carry_u = 0, carry_p = 0;
-        for (int base = 0; base < E; base += 32) {
-            const int e = base + lane;
+    // Exclusive scans over the experts of (count > 0) and count, 32 experts per warp
+    // chunk: chunk totals first, then each chunk's prefix from ballots (an expert's
+    // count is at most M <= 16, so five bit planes give the count prefix) plus the
+    // totals of the chunks before it.
+    {
+        __shared__ int tot_u[kMoeMaxE / 32], tot_p[kMoeMaxE / 32];
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+        const int chunks = (E + 31) / 32;
+        const unsigned lt = (1u << lane) - 1u;
+        for (int ch = warp; ch < chunks; ch += nw) {
+            const int e = ch * 32 + lane;
             const int c = e < E ? R.cnt[e] : 0;
-            const int a = c > 0 ? 1 : 0;
-            int su = a, sp = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int nu = __shfl_up_sync(kFull, su, o);
-                const int np = __shfl_up_sync(kFull, sp, o);
-                if (lane >= o) {
-                    su += nu;
-                    sp += np;
-                }
+            const unsigned act = __ballot_sync(kFull, c > 0);
+            const int sum = __reduce_add_sync(kFull, static_cast<unsigned>(c));
+            if (lane == 0) {
+                tot_u[ch] = __popc(act);
+                tot_p[ch] = sum;
             }
-            const int ex_u = carry_u + su - a, ex_p = carry_p + sp - c;
+        }
+        __syncthreads();
+        for (int ch = warp; ch < chunks; ch += nw) {
+            int carry_u = 0, carry_p = 0;
+            for (int j = 0; j < ch; ++j) {
+                carry_u += tot_u[j];
+                carry_p += tot_p[j];
+            }
+            const int e = ch * 32 + lane;
+            const int c = e < E ? R.cnt[e] : 0;
+            const unsigned act = __ballot_sync(kFull, c > 0);
+            int ex_p = 0;
+#pragma unroll
+            for (int b = 0; b < 5; ++b) ex_p += __popc(__ballot_sync(kFull, (c >> b) & 1) & lt) << b;
+            const int ex_u = carry_u + __popc(act & lt);
+            ex_p += carry_p;
             if (e < E) {
-                if (a) {
+                if (c > 0) {
                     R.experts[ex_u] = static_cast<int16_t>(e);
                     R.offs[ex_u] = static_cast<int16_t>(ex_p);
                 }
                 R.cnt[e] = ex_p;    // now the expert's first pair position
             }
-            carry_u += __shfl_sync(kFull, su, 31);
-            carry_p += __shfl_sync(kFull, sp, 31);
-        }
-        if (lane == 0) {
-            R.U = carry_u;
-            R.P = carry_p;
-            R.offs[carry_u] = static_cast<int16_t>(carry_p);
+            if (ch == chunks - 1 && lane == 31) {
+                R.U = ex_u + (c > 0 ? 1 : 0);
+                R.P = ex_p + c;
+                R.offs[R.U] = static_cast<int16_t>(R.P);
+            }
         }
     }
     __syncthreads();
