@@ -38,6 +38,7 @@ SWEEP_NK = [(4096, 4096), (12288, 4096), (4096, 12288), (32768, 1024), (8192, 40
 SWEEP_M = [1, 2, 4, 8, 16, 32, 64, 128]
 GATE_UP_M = [1, 2, 3, 4, 6, 8, 12, 16, 32, 64, 128]
 HEAD_M = [1, 2, 3, 4, 8]
+CHAIN_M = [1, 2, 4, 8, 16]
 MOE_M = [1, 2, 4, 8, 16]
 MOE_E, MOE_I, MOE_K, MOE_TOPK = 128, 1536, 4096, 6
 HEAD_N, HEAD_K = 248320, 4096
@@ -171,13 +172,16 @@ def run_gpu(args):
     def wanted(name, meta):
         return pattern is None or pattern.search(case_id(name, meta)) is not None
 
-    def add(name, meta, calls, wbytes):
+    kernels = []      # kernel launches of one call of each case
+
+    def add(name, meta, calls, wbytes, launches_per_call=1):
         if not wanted(name, meta):
             return
         with torch.cuda.stream(stream):
             g = _graph_case(torch, calls, R, stream)
         cases.append((name, meta, g, wbytes))
         keep.append(calls)
+        kernels.append(launches_per_call)
 
     # --- the headline sweep
     sweep_cases = []
@@ -256,6 +260,43 @@ def run_gpu(args):
                 [(lambda r=r, a=a, yv=yv, ws2=ws2, W2q=W2q, s2=s2: dg.dg_moe_w2(a, r[1], r[2], W2q, s2, yv, ws=ws2, stream=stream))
                  for r in routs], b2)
 
+        # --- chained pairs inside one graph (PDL lets the second kernel's prologue and
+        #     first weight loads overlap the first one's tail): MLP gate/up -> down
+        #     projection, and MoE W1 -> W2
+        if need("chain_mlp", [{"M": M} for M in CHAIN_M]) and Ws:
+            Nh, K = 12288, 4096
+            Wd0 = S.linear_inputs(1, 4096, Nh, device=dev)[1]
+            Wds = [Wd0, Wd0.clone()]
+            for M in CHAIN_M:
+                x = S.gate_up_inputs(M, Nh, K, device=dev)[0]
+                h = torch.empty((M, Nh), dtype=torch.bfloat16, device=dev)
+                yd = torch.empty((M, 4096), dtype=torch.bfloat16, device=dev)
+                wsa = dg.workspace(dg.DG_OP_GATE_UP_SILU, M, Nh, K, device=dev)
+                wsb = dg.workspace(dg.DG_OP_GEMV_BF16, M, 4096, Nh, device=dev)
+
+                def pair(W, Wd, x=x, h=h, yd=yd, wsa=wsa, wsb=wsb):
+                    dg.dg_gate_up_silu(x, W, h, ws=wsa, stream=stream)
+                    dg.dg_gemv_bf16(h, Wd, yd, ws=wsb, stream=stream)
+                add("chain_mlp", {"M": M},
+                    [(lambda i=i, f=pair, wg=Ws, wd=Wds: f(wg[i % len(wg)], wd[i % 2]))
+                     for i in range(max(len(Ws), 2))],
+                    2 * Nh * K * 2 + 4096 * Nh * 2, launches_per_call=2)
+        if moe_on and need("chain_moe", [{"M": M} for M in MOE_M]):
+            for M in MOE_M:
+                routs = [S.moe_inputs(M, MOE_K, MOE_TOPK, MOE_E, rep=r, device=dev) for r in range(8)]
+                uniq = [len(set(r[1].cpu().flatten().tolist())) for r in routs]
+                u_mean = sum(uniq) / len(uniq)
+                a = torch.empty((M, MOE_TOPK, MOE_I), dtype=torch.bfloat16, device=dev)
+                yv = torch.empty((M, MOE_K), dtype=torch.bfloat16, device=dev)
+                ws1 = dg.workspace(dg.DG_OP_MOE_W1, M, MOE_I, MOE_K, MOE_TOPK, device=dev)
+                ws2 = dg.workspace(dg.DG_OP_MOE_W2, M, MOE_K, MOE_I, MOE_TOPK, device=dev)
+
+                def pair(r, a=a, yv=yv, ws1=ws1, ws2=ws2):
+                    dg.dg_moe_w1_silu(r[0], r[1], W1q, s1, a, ws=ws1, stream=stream)
+                    dg.dg_moe_w2(a, r[1], r[2], W2q, s2, yv, ws=ws2, stream=stream)
+                add("chain_moe", {"M": M, "U_mean": u_mean}, [(lambda r=r, f=pair: f(r)) for r in routs],
+                    u_mean * (3 * MOE_I * MOE_K + 2 * MOE_I * 4 + MOE_K * 4), launches_per_call=2)
+
     n_cases = len(cases)
     if n_cases == 0:
         raise SystemExit(f"no benchmark case matches --cases {args.cases!r} / --only {args.only!r}")
@@ -292,6 +333,32 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
+
+    # ---- cold single calls (outside the timed region): L2 flushed before each call
+    cold = None
+    if not args.no_cold and sweep_cases:
+        flush = torch.empty(max(2 * l2, 1 << 28), dtype=torch.uint8, device=dev)
+        cev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        cold_us = {}
+        with torch.cuda.stream(stream):
+            for i in sweep_cases:
+                call = keep[i][0]
+                ts = []
+                for _ in range(5):
+                    flush.fill_(1)
+                    cev[0].record(stream)
+                    call()
+                    cev[1].record(stream)
+                    stream.synchronize()
+                    ts.append(cev[0].elapsed_time(cev[1]) * 1e3)
+                cold_us[i] = statistics.median(ts)
+        del flush
+        cb = sum(cases[i][3] for i in sweep_cases)
+        ct = sum(cold_us.values())
+        cold = {"value": round(cb / (ct * 1e-6) / 1e9, 1), "unit": "GB/s", "us_per_step": round(ct, 1),
+                "method": "each sweep call alone, eager, after writing a 2xL2 buffer; CUDA events around "
+                          "the call on its stream; median of 5",
+                "us": {case_id(cases[i][0], cases[i][1]): round(cold_us[i], 3) for i in sweep_cases}}
 
     def summarize(i):
         name, meta, _, wb = cases[i]
@@ -334,11 +401,23 @@ def run_gpu(args):
             continue
         s = summarize(i)
         ops.setdefault(s["op"], []).append(s)
+    # chained pairs: the same two calls measured on their own, for the PDL overlap
+    sweep_by = {(s_["M"], s_["N"], s_["K"]): s_["us"] for s_ in sweep if "N" in s_}
+    for c in ops.get("chain_mlp", []):
+        gu = next((o["us"] for o in ops.get("gate_up_silu", []) if o["M"] == c["M"]), None)
+        dn = sweep_by.get((c["M"], 4096, 12288))
+        if gu is not None and dn is not None:
+            c["parts_us"] = round(gu + dn, 3)
+    for c in ops.get("chain_moe", []):
+        w1 = next((o["us"] for o in ops.get("moe_w1_silu", []) if o["M"] == c["M"]), None)
+        w2 = next((o["us"] for o in ops.get("moe_w2", []) if o["M"] == c["M"]), None)
+        if w1 is not None and w2 is not None:
+            c["parts_us"] = round(w1 + w2, 3)
 
     # ---- e2e through the public API with host buffers (x in, y out, pinned)
     e2e = _e2e(torch, dg, S, dev, stream, args, l2) if only is None and not args.cases else None
 
-    launches = args.steps * R * n_cases
+    launches = args.steps * R * sum(kernels)
     res = {
         "metric": METRIC,
         "value": round(value, 1),
@@ -372,6 +451,7 @@ def run_gpu(args):
                                       if small else None)},
         "clocks": clk,
         "e2e": e2e,
+        "cold": cold,
         "gpu_launches": launches,
         "shapes": sweep,
         "ops": ops,
@@ -517,11 +597,26 @@ def _oracle_sweep_sample(budget_s: float, rows_frac: int = 8):
     return total_b, total_t, f"{passes} pass(es) over every {rows_frac}th weight row of all 40 sweep shapes"
 
 
+def _cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (x86 'model name', or Arm implementer/part)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    for key in ("model name", "Model", "CPU part"):
+        m = re.search(rf"^{key}\s*:\s*(.+)$", info, re.M)
+        if m:
+            return (key + " " if key == "CPU part" else "") + m.group(1).strip()
+    return "unknown"
+
+
 def cpu_baseline(budget_s: float):
     b, t, sample = _oracle_sweep_sample(budget_s)
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return {"value": round(b / t / 1e9, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": sample + f"; {t:.1f} s of fp64 oracle work, GB/s of weight bytes covered"}
+            "cpu_model": _cpu_model(), "nproc": os.cpu_count(),
+            "sample": sample + f"; {t:.1f} s of fp64 oracle work (OpenMP over outputs, {cores} threads), "
+                               "GB/s of weight bytes covered"}
 
 
 def run_reference(args):
@@ -546,6 +641,7 @@ def run_reference(args):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": WORKLOAD},
            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                            "cpu_model": _cpu_model(), "nproc": os.cpu_count(),
                             "sample": sample},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
@@ -561,6 +657,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--sweep-only", action="store_true", help="only the headline sweep (no other ops)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cold", action="store_true", help="skip the cold single-call timings")
     ap.add_argument("--only", default="", help="profiling: one sweep shape 'M,N,K' (no other ops, no e2e)")
     ap.add_argument("--cases", default="", help="profiling: regex over case ids such as 'moe_w2/M16' or "
                     "'head_fp8_argmax/M8/N248320/K4096' (only matching cases are built and timed)")

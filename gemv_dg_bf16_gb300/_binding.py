@@ -87,6 +87,8 @@ def lib():
     L.dg_device_status_clear.argtypes = [P, P]
     L.dg_selftest_wait_timeout.argtypes = [P, I, P]
     L.dg_selftest_wait_timeout.restype = S
+    L.dg_moe_route_debug.argtypes = [P, I, I, I, P, P, P]
+    L.dg_moe_route_debug.restype = S
     L.dg_set_launch_flags.argtypes = [ctypes.c_uint]
     L.dg_set_launch_flags.restype = S
     L.dg_launch_flags.argtypes = []
@@ -165,6 +167,31 @@ def dg_launch_flags() -> int:
 
 def dg_selftest_wait_timeout(ws, timeout_us: int = 20000, stream=None):
     _ok(lib().dg_selftest_wait_timeout(_ptr(ws), int(timeout_us), _stream(stream)), "dg_selftest_wait_timeout")
+
+
+DG_ROUTE_DEBUG_INTS = 2 + 128 + 16 + 128 + 129 + 128 + 128
+
+
+def dg_moe_route_debug(topk_ids, E: int, ws=None, stream=None) -> dict:
+    """The MoE kernels' routing tables for topk_ids [M, topk] (device int32), as numpy."""
+    _check_dev(topk_ids)
+    M, topk = topk_ids.shape
+    out = torch.empty(DG_ROUTE_DEBUG_INTS, dtype=torch.int32, device=topk_ids.device)
+    if ws is None:
+        ws = torch.zeros(256, dtype=torch.uint8, device=topk_ids.device)
+    _ok(lib().dg_moe_route_debug(_ptr(topk_ids), M, topk, int(E), _ptr(out), _ptr(ws), _stream(stream)),
+        "dg_moe_route_debug")
+    o = out.cpu().numpy()
+    U, P = int(o[0]), int(o[1])
+    valid = o[2:2 + 128]
+    nvalid = o[130:146]
+    experts = o[146:274]
+    offs = o[274:403]
+    ptok = o[403:531]
+    pslot = o[531:659]
+    return dict(U=U, P=P, valid=valid[:M * topk].reshape(M, topk).copy(), nvalid=nvalid[:M].copy(),
+                experts=experts[:U].copy(), offsets=offs[:U + 1].copy(), pair_tok=ptok[:P].copy(),
+                pair_slot=pslot[:P].copy())
 
 
 def dg_workspace_bytes(op: int, M: int, N: int, K: int, topk: int = 0) -> int:

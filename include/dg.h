@@ -149,6 +149,23 @@ dg_status dg_device_status_clear(void* ws, dg_stream_t stream);
  * runs out.  Asynchronous on `stream`; the context stays usable. */
 dg_status dg_selftest_wait_timeout(void* ws, int timeout_us, dg_stream_t stream);
 
+/* Test export of the MoE routing step ("Decode optimization round 3", Retained
+ * change 1: the active experts and their (token, slot) pairs): one CTA runs the
+ * routing scan the MoE kernels run and writes, into the caller's device buffer
+ * `out` of DG_ROUTE_DEBUG_INTS int32 (asynchronously on `stream`):
+ *   [0] U active experts, [1] P valid pairs,
+ *   [2 .. 2+128)          valid[t*topk + k] (1/0; 0 past M*topk),
+ *   then 16               valid slots per token (0 past M),
+ *   then 128              active experts ascending (-1 past U),
+ *   then 129              pair offsets of each active expert, offs[U] = P (-1 past U),
+ *   then 128 + 128        pair token / pair slot, by expert then token then slot (-1 past P).
+ * topk_ids [M, topk] int32 device; 1 <= M <= 16, 1 <= topk <= 8, 1 <= E <= 1024;
+ * ws a zero-filled workspace (its status word gets DG_DEVERR_BAD_TOPK_ID for
+ * invalid slots).  Argument errors return before any launch. */
+#define DG_ROUTE_DEBUG_INTS (2 + 128 + 16 + 128 + 129 + 128 + 128)
+dg_status dg_moe_route_debug(const int32_t* topk_ids, int M, int topk, int E, int32_t* out, void* ws,
+                             dg_stream_t stream);
+
 /* ---------------------------------------------------------------- compute */
 
 /* Decode linear, mstar PR #1104 (decode GEMM table), "Why" / "What changed":

@@ -179,3 +179,35 @@ def test_moe_single_expert_equals_scaled_gemv(cuda_device, family):
     s = s2[2].cpu().numpy().astype(np.float64)
     exc = T.linear_excess(f64(y), lg * s, ad * s)
     assert (exc <= 0).all()
+
+
+@pytest.mark.parametrize("M,E,seed,bad", [(1, 128, 1, False), (2, 128, 2, False), (5, 8, 3, True), (7, 128, 4, True),
+                                          (16, 128, 5, False), (16, 16, 6, True), (3, 1000, 7, True)])
+def test_moe_routing_tables_match_oracle(cuda_device, M, E, seed, bad):
+    """The routing scan the MoE kernels run, exported, equals the oracle's grouping bit for bit."""
+    topk = 6
+    ids, _ = S.moe_routing(M, topk, E, seed=seed)
+    if bad:                                   # repeated and out-of-range ids
+        g = torch.Generator().manual_seed(seed)
+        for _ in range(max(1, M)):
+            t, k = int(torch.randint(M, (1,), generator=g)), int(torch.randint(topk, (1,), generator=g))
+            ids[t, k] = [-1, E, E + 7, int(ids[t, 0])][int(torch.randint(4, (1,), generator=g))]
+    ws = dg.workspace(dg.DG_OP_MOE_W1, M, 64, 64, topk)
+    r = dg.dg_moe_route_debug(ids.to(cuda_device), E, ws=ws)
+    ref = O.moe_route(ids.numpy(), E)
+    assert np.array_equal(r["valid"], ref["valid"])
+    assert np.array_equal(r["nvalid"], ref["valid"].sum(axis=1))
+    assert np.array_equal(r["experts"], ref["experts"]) and r["U"] == len(ref["experts"])
+    assert np.array_equal(r["offsets"], ref["offsets"]) and r["P"] == int(ref["offsets"][-1])
+    assert np.array_equal(r["pair_tok"], ref["pair_tok"])
+    assert np.array_equal(r["pair_slot"], ref["pair_slot"])
+    assert bool(dg.dg_device_status(ws) & dg.DG_DEVERR_BAD_TOPK_ID) == bool((ref["valid"] == 0).any())
+
+
+def test_moe_routing_export_rejects_bad_arguments(cuda_device):
+    ids = torch.zeros((2, 6), dtype=torch.int32, device=cuda_device)
+    for kw in (dict(E=0), dict(E=2000)):
+        with pytest.raises(dg.DGError):
+            dg.dg_moe_route_debug(ids, **kw)
+    with pytest.raises(dg.DGError):
+        dg.dg_moe_route_debug(torch.zeros((17, 6), dtype=torch.int32, device=cuda_device), 128)
