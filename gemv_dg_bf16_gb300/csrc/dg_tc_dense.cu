@@ -98,22 +98,6 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr)
     return v;
 }
 
-// Final value of (row n, token t) -> output.  Gate/up: even rows are gate rows,
-// odd rows up rows; lanes hold consecutive rows, so the up value is one lane up.
-template <int EPI>
-__device__ __forceinline__ void emit(const TcArgs& a, int t, int n, float v, bool valid)
-{
-    if constexpr (EPI == 0) {
-        if (valid) a.out[static_cast<size_t>(t) * a.ld_out + n] = f32_to_bf16_bits(v);
-    } else {
-        const float u = __shfl_down_sync(kFull, v, 1);
-        if (valid && (n % 2) == 0) {
-            const float silu = v / (1.0f + expf(-v));
-            a.out[static_cast<size_t>(t) * a.ld_out + n / 2] = f32_to_bf16_bits(silu * u);
-        }
-    }
-}
-
 // Four consecutive rows n..n+3 of token t held by one thread (n a multiple of 4).
 template <int EPI>
 __device__ __forceinline__ void emit4(const TcArgs& a, int t, int n, float4 v)
@@ -136,6 +120,65 @@ __device__ __forceinline__ void emit4(const TcArgs& a, int t, int n, float4 v)
         uint16_t* dst = a.out + static_cast<size_t>(t) * a.ld_out + n / 2;
         if (n + 1 < a.N) dst[0] = f32_to_bf16_bits(s0 * v.y);
         if (n + 3 < a.N) dst[1] = f32_to_bf16_bits(s1 * v.w);
+    }
+}
+
+// Rows [r0, r1) (multiples of 4) of a tile's final fp32 values, staged in shared
+// memory as S[t][r - r0] (row stride rs, a multiple of 4), written out by the 128
+// epilogue threads (etid) in 8-row pieces (16 bytes of bf16) -- 4-row pieces (the
+// 8-byte path of emit4) when the range does not start and end on 8-row boundaries:
+// consecutive threads take consecutive pieces of one token's output row, so every
+// warp store is contiguous.
+template <int EPI>
+__device__ __forceinline__ void store_staged(const TcArgs& a, const float* S, int rs, int tile, int r0, int r1,
+                                             int etid)
+{
+    // 16-byte pieces need the range to start on an 8-row boundary (rank slices may
+    // start at any multiple of 4) and to hold whole 8-row pieces.
+    if ((r1 - r0) % 8 != 0 || (r0 % 8) != 0) {
+        const int q4 = (r1 - r0) / 4;
+#pragma unroll 1
+        for (int i = etid; i < a.M * q4; i += 128) {
+            const int t = i / q4, c = i - t * q4;
+            emit4<EPI>(a, t, tile * kTileRows + r0 + c * 4, *reinterpret_cast<const float4*>(S + t * rs + c * 4));
+        }
+        return;
+    }
+    const int q = (r1 - r0) / 8;                      // 8-row pieces per token
+    const int n0 = tile * kTileRows + r0;
+    const bool vec = EPI == 0 ? (a.ld_out % 8) == 0 : (a.ld_out % 4) == 0;
+#pragma unroll 1
+    for (int i = etid; i < a.M * q; i += 128) {
+        const int t = i / q, c = i - t * q;
+        const float* src = S + t * rs + c * 8;
+        const float4 lo = *reinterpret_cast<const float4*>(src);
+        const float4 hi = *reinterpret_cast<const float4*>(src + 4);
+        const int n = n0 + c * 8;
+        if constexpr (EPI == 0) {
+            if (vec && n + 7 < a.N) {
+                uint4 w;
+                w.x = f32_to_bf16_bits(lo.x) | (static_cast<uint32_t>(f32_to_bf16_bits(lo.y)) << 16);
+                w.y = f32_to_bf16_bits(lo.z) | (static_cast<uint32_t>(f32_to_bf16_bits(lo.w)) << 16);
+                w.z = f32_to_bf16_bits(hi.x) | (static_cast<uint32_t>(f32_to_bf16_bits(hi.y)) << 16);
+                w.w = f32_to_bf16_bits(hi.z) | (static_cast<uint32_t>(f32_to_bf16_bits(hi.w)) << 16);
+                *reinterpret_cast<uint4*>(a.out + static_cast<size_t>(t) * a.ld_out + n) = w;
+            } else {
+                emit4<0>(a, t, n, lo);
+                emit4<0>(a, t, n + 4, hi);
+            }
+        } else {
+            if (vec && n + 7 < a.N) {
+                const float g0 = lo.x / (1.0f + expf(-lo.x)), g1 = lo.z / (1.0f + expf(-lo.z));
+                const float g2 = hi.x / (1.0f + expf(-hi.x)), g3 = hi.z / (1.0f + expf(-hi.z));
+                uint2 w;
+                w.x = f32_to_bf16_bits(g0 * lo.y) | (static_cast<uint32_t>(f32_to_bf16_bits(g1 * lo.w)) << 16);
+                w.y = f32_to_bf16_bits(g2 * hi.y) | (static_cast<uint32_t>(f32_to_bf16_bits(g3 * hi.w)) << 16);
+                *reinterpret_cast<uint2*>(a.out + static_cast<size_t>(t) * a.ld_out + n / 2) = w;
+            } else {
+                emit4<1>(a, t, n, lo);
+                emit4<1>(a, t, n + 4, hi);
+            }
+        }
     }
 }
 
@@ -240,70 +283,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Epilogue warps 2..5 -> TMEM lane quarter (warp % 4).
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        const int n = tile * kTileRows + row;
         const bool ok = tc::bar_wait(accum, 0, abort_flag);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        if (!ok || *abort_flag) {
-            if (row == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
-        } else if (!clustered) {
+        // `good` may differ between threads when a wait ran out; every named barrier
+        // below is still reached by all 128 epilogue threads.
+        const bool good = ok && !*abort_flag;
+        if (!good && row == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
+        if (!clustered) {
+            // Stage the tile S[t][row] (fp32) in the now idle stage memory, then write
+            // it out in coalesced 16-byte pieces.
+            float* S = reinterpret_cast<float*>(smem);
+            if (good) {
 #pragma unroll 1
-            for (int c = 0; c < MP / 16; ++c) {
-                uint32_t v[16];
-                tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
+                for (int c = 0; c < MP / 16 && c * 16 < a.M; ++c) {
+                    uint32_t v[16];
+                    tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const int t = c * 16 + j;
-                    emit<EPI>(a, t, n, __uint_as_float(v[j]), t < a.M && n < a.N);
+                    for (int j = 0; j < 16; ++j)
+                        if (c * 16 + j < a.M) S[(c * 16 + j) * kTileRows + row] = __uint_as_float(v[j]);
                 }
             }
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (good) store_staged<EPI>(a, S, kTileRows, tile, 0, kTileRows, threadIdx.x - 64);
         } else if (a.push) {
             // Push row `row` of this rank's partial tile (tokens 0..mq-1) into the
             // shared memory of the rank that folds it.
-            int owner = 0;
-            while (owner + 1 < a.nsplit && row >= slice_lo(owner + 1, a.nsplit)) ++owner;
-            const uint32_t dst = map_to_rank(tc::su32(recv), static_cast<uint32_t>(owner)) +
-                                 static_cast<uint32_t>(((split * a.slice_max + row - slice_lo(owner, a.nsplit)) * a.mq) * 4);
-            const uint32_t dbar = map_to_rank(recv_bar, static_cast<uint32_t>(owner));
+            if (good) {
+                int owner = 0;
+                while (owner + 1 < a.nsplit && row >= slice_lo(owner + 1, a.nsplit)) ++owner;
+                const uint32_t dst = map_to_rank(tc::su32(recv), static_cast<uint32_t>(owner)) +
+                                     static_cast<uint32_t>(((split * a.slice_max + row - slice_lo(owner, a.nsplit)) * a.mq) * 4);
+                const uint32_t dbar = map_to_rank(recv_bar, static_cast<uint32_t>(owner));
 #pragma unroll 1
-            for (int c = 0; c < MP / 16 && c * 16 < a.mq; ++c) {
-                uint32_t v[16];
-                tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
+                for (int c = 0; c < MP / 16 && c * 16 < a.mq; ++c) {
+                    uint32_t v[16];
+                    tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
 #pragma unroll
-                for (int j = 0; j < 16; j += 4)
-                    if (c * 16 + j < a.mq)
-                        st_async_f32x4(dst + (c * 16 + j) * 4, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                       __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), dbar);
+                    for (int j = 0; j < 16; j += 4)
+                        if (c * 16 + j < a.mq)
+                            st_async_f32x4(dst + (c * 16 + j) * 4, __uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                           __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]), dbar);
+                }
             }
-            // This rank's slice: wait for every rank's rows, fold them in rank order.
+            // This rank's slice: wait for every rank's rows, fold them in rank order into
+            // S[t][r] (the idle stage memory), then coalesced stores.
             const int lo = slice_lo(split, a.nsplit), hi = slice_lo(split + 1, a.nsplit);
-            const bool got = tc::bar_wait(recv_bar, 0, abort_flag);
-            if (got) {
-                const int r = threadIdx.x - 64;            // 0..127: one folded row per thread
-                const bool mine = r < hi - lo;
-                const int nr = tile * kTileRows + lo + r;
+            const bool got = good && tc::bar_wait(recv_bar, 0, abort_flag);
+            if (good && !got && row == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
+            const int r = threadIdx.x - 64;                // 0..127: one folded row per thread
+            float* S = reinterpret_cast<float*>(smem);
+            const int rs = a.slice_max;
+            if (got && r < hi - lo) {
 #pragma unroll 1
                 for (int t = 0; t < a.mq; t += 4) {
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (mine) {
-                        acc = *reinterpret_cast<const float4*>(recv + (static_cast<size_t>(r) * a.mq + t));
-                        for (int s2 = 1; s2 < a.nsplit; ++s2) {
-                            const float4 v = *reinterpret_cast<const float4*>(
-                                recv + ((static_cast<size_t>(s2) * a.slice_max + r) * a.mq + t));
-                            acc.x = acc.x + v.x;
-                            acc.y = acc.y + v.y;
-                            acc.z = acc.z + v.z;
-                            acc.w = acc.w + v.w;
-                        }
+                    float4 acc = *reinterpret_cast<const float4*>(recv + (static_cast<size_t>(r) * a.mq + t));
+                    for (int s2 = 1; s2 < a.nsplit; ++s2) {
+                        const float4 v = *reinterpret_cast<const float4*>(
+                            recv + ((static_cast<size_t>(s2) * a.slice_max + r) * a.mq + t));
+                        acc.x = acc.x + v.x;
+                        acc.y = acc.y + v.y;
+                        acc.z = acc.z + v.z;
+                        acc.w = acc.w + v.w;
                     }
-                    emit<EPI>(a, t + 0, nr, acc.x, mine && t + 0 < a.M && nr < a.N);
-                    emit<EPI>(a, t + 1, nr, acc.y, mine && t + 1 < a.M && nr < a.N);
-                    emit<EPI>(a, t + 2, nr, acc.z, mine && t + 2 < a.M && nr < a.N);
-                    emit<EPI>(a, t + 3, nr, acc.w, mine && t + 3 < a.M && nr < a.N);
+                    S[(t + 0) * rs + r] = acc.x;
+                    S[(t + 1) * rs + r] = acc.y;
+                    S[(t + 2) * rs + r] = acc.z;
+                    S[(t + 3) * rs + r] = acc.w;
                 }
-            } else if (row == 0) {
-                set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
             }
-        } else {
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (got && !*abort_flag) store_staged<EPI>(a, S, rs, tile, lo, hi, r);
+        } else if (good) {
             // Park this rank's partial tile P[t][row] (fp32) in the now idle stage memory.
             float* P = reinterpret_cast<float*>(smem);
 #pragma unroll 1
