@@ -31,6 +31,7 @@ constexpr unsigned kFull = 0xffffffffu;
 // ordered on one stream); each op leaves its counters at zero when it finishes.
 constexpr size_t kWsStatus = 0;            // int32 sticky device status word
 constexpr size_t kWsTicket = 16;           // uint32 ticket of single-ticket kernels (the head)
+constexpr size_t kWsGridBarrier = 24;      // uint32 counter + generation of a grid barrier (tensor-core MoE W2)
 constexpr size_t kWsCounters = 256;        // uint32 tickets of multi-ticket kernels (TC tiles, MoE)
 constexpr size_t kWsData = 32768;          // per-op scratch data starts here
 constexpr int kWsMaxCounters = static_cast<int>((kWsData - kWsCounters) / 4);

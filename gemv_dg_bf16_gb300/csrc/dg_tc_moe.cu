@@ -12,8 +12,9 @@
 // activations only when its expert (or pair chunk) changes.
 //   W1 tile: 64 gate rows j0.. and the 64 matching up rows I + j0.. (two TMA boxes);
 //            a[t, k, j] = bf16(silu(g * s1[e, j]) * (u * s1[e, I + j]))
-//   W2 tile: 128 output rows n0..; (h * s2[e, n]) * gw[t, k] go to the workspace and
-//            the CTA that completes a (token, tile) ticket folds the slots in order.
+//   W2 tile: 128 output rows n0..; (h * s2[e, n]) * gw[t, k] go to the workspace;
+//            after one grid barrier (the grid is one resident CTA per SM) every
+//            CTA folds a share of the outputs over the valid slots in slot order.
 //   warp 0     TMA producer (weights only, ring of stages)
 //   warp 1     TMEM allocation, MMA issue (lane 0)
 //   warps 2-5  split activations for each pass, epilogue of each tile
@@ -48,6 +49,33 @@ struct TcMoeArgs {
     int stages;
 };
 
+// Sense-reversing grid barrier for a grid whose CTAs are all resident: counter at
+// bar[0], generation at bar[1] (in the workspace header; the last arriver resets
+// the counter for the next call).  Bounded: false after kWaitNs or
+// when this CTA already aborted.
+__device__ inline bool grid_barrier(unsigned* bar, volatile int* abort_flag)
+{
+    volatile unsigned* gen = bar + 1;
+    const unsigned my_gen = *gen;
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+        bar[0] = 0u;
+        __threadfence();
+        atomicAdd(bar + 1, 1u);
+        return true;
+    }
+    unsigned long long t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (uint32_t i = 1;; ++i) {
+        if (*gen != my_gen) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            unsigned long long t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            if (t - t0 > kWaitNs) return false;
+        }
+    }
+}
+
 template <bool W1>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_moe_kernel(const __grid_constant__ CUtensorMap tmW, TcMoeArgs A)
@@ -66,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float red[4][kPairs];
     __shared__ float sig[kPairs], isig[kPairs];
     __shared__ float exch[kPairs][64];       // W1: up values of a tile's 64 columns
-    __shared__ int8_t fold_tok[kPairs];   // W2: pairs of the pass whose token this pass folds
+    __shared__ int grid_ok;                   // W2: the grid barrier completed
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     pdl_launch_dependents();
@@ -177,7 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int et = threadIdx.x - 64;          // 0..127
         const int q = warp & 3;                   // TMEM lane quarter
         const int row = q * 32 + lane;
-        unsigned* tickets = reinterpret_cast<unsigned*>(a.ws + kWsCounters);
         float* terms = reinterpret_cast<float*>(a.ws + kWsData);
         int jt = 0;
         for_each_pass([&](int ue, int p0, int c, int t_lo, int t_hi) {
@@ -269,51 +296,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                             terms[(static_cast<size_t>(t) * a.topk + k) * a.Nout + n] = h * a.gw[t * a.topk + k];
                         }
                     }
-                    // Publish, then take every pair's (token, tile) ticket at once (one
-                    // thread per pair; the pairs of a pass are distinct tokens); fold the
-                    // tokens whose last term this was, in slot order.
-                    __threadfence();
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    if (et < c) {
-                        const int t = R.ptok[p0 + et];
-                        const unsigned old = atomicAdd(&tickets[t * T + tile], 1u);
-                        fold_tok[et] = (old + 1 == static_cast<unsigned>(R.nvalid[t])) ? 1 : 0;
-                    }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    bool any = false;
-                    for (int p = 0; p < c; ++p) {
-                        if (!fold_tok[p]) continue;
-                        if (!any) __threadfence();
-                        any = true;
-                        const int t = R.ptok[p0 + p];
-                        if (n < a.Nout) {
-                            float y = 0.0f;
-                            bool first = true;
-                            for (int k = 0; k < a.topk; ++k) {
-                                if (!R.valid[t * a.topk + k]) continue;
-                                const float tv = ld_cg_f32(terms + (static_cast<size_t>(t) * a.topk + k) * a.Nout + n);
-                                y = first ? tv : y + tv;
-                                first = false;
-                            }
-                            a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
-                        }
-                        if (et == 0) tickets[t * T + tile] = 0u;
-                    }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");    // fold_tok reuse
                 }
             }
             return true;
         });
-        // Invalid slots (W1) and tokens without a valid slot (W2) are written by CTA 0.
-        if (blockIdx.x == 0) {
-            if constexpr (W1) {
+        if constexpr (W1) {
+            // Invalid slots get a = 0 (no unit covers them), written by CTA 0.
+            if (blockIdx.x == 0)
                 for (int i = 0; i < a.M * a.topk; ++i)
                     if (!R.valid[i])
                         for (int j = et; j < a.I; j += 128) a.out[static_cast<size_t>(i) * a.I + j] = 0;
-            } else {
-                for (int t = 0; t < a.M; ++t)
-                    if (R.nvalid[t] == 0)
-                        for (int n = et; n < a.Nout; n += 128) a.out[static_cast<size_t>(t) * a.Nout + n] = 0;
+        } else {
+            // Combine: once every CTA has written its terms (one grid barrier; the grid
+            // is one CTA per SM, and a dependent launch starts only after all of them
+            // have started, so all are resident), the outputs are folded in slot order,
+            // spread over every CTA's epilogue threads.  Tokens without a valid slot
+            // get y = 0.
+            __threadfence();
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (et == 0) grid_ok = grid_barrier(reinterpret_cast<unsigned*>(a.ws + kWsGridBarrier), abort_flag) ? 1 : 0;
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (grid_ok) {
+                __threadfence();
+                const long total = static_cast<long>(a.M) * a.Nout;
+                for (long i = static_cast<long>(blockIdx.x) * 128 + et; i < total; i += static_cast<long>(gridDim.x) * 128) {
+                    const int t = static_cast<int>(i / a.Nout), n = static_cast<int>(i - static_cast<long>(t) * a.Nout);
+                    float y = 0.0f;
+                    bool first = true;
+                    for (int k = 0; k < a.topk; ++k) {
+                        if (!R.valid[t * a.topk + k]) continue;
+                        const float tv = ld_cg_f32(terms + (static_cast<size_t>(t) * a.topk + k) * a.Nout + n);
+                        y = first ? tv : y + tv;
+                        first = false;
+                    }
+                    a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
+                }
+            } else if (et == 0) {
+                set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
             }
         }
     }
@@ -347,7 +366,6 @@ dg_status launch_tc_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, cons
     if (stages < 2 || stages > 16 || smem_bytes(nkb, stages) > kMaxDynSmem) return DG_ERR_BAD_VARIANT;
     if (w1 && m.I % 64 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
     const int T = w1 ? m.I / 64 : (m.Nout + kRows - 1) / kRows;
-    if (!w1 && m.M * T > kWsMaxCounters) return DG_ERR_UNSUPPORTED_SHAPE;
     std::call_once(g_once, [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
