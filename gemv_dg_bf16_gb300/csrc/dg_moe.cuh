@@ -137,4 +137,34 @@ __device__ inline void route_scan(Route& R, const int32_t* __restrict__ ids, int
     __syncthreads();
 }
 
+// Sense-reversing grid barrier for a grid whose CTAs are all resident at once (a
+// persistent grid sized by the occupancy; a dependent launch starts only after
+// every CTA of this one has started, so none of them can be kept off an SM by it).
+// Counter at bar[0], generation at bar[1]; the last arriver resets the counter for
+// the next call.  One thread per CTA calls it.  Bounded: false after 2 s, or at
+// once when `abort_flag` (if given) is raised.
+__device__ inline bool grid_barrier(unsigned* bar, volatile int* abort_flag = nullptr)
+{
+    constexpr unsigned long long kLimitNs = 2000000000ull;
+    volatile unsigned* gen = bar + 1;
+    const unsigned my_gen = *gen;
+    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
+        bar[0] = 0u;
+        __threadfence();
+        atomicAdd(bar + 1, 1u);
+        return true;
+    }
+    unsigned long long t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+    for (uint32_t i = 1;; ++i) {
+        if (*gen != my_gen) return true;
+        if ((i & 63u) == 0) {
+            if (abort_flag && *abort_flag) return false;
+            unsigned long long t;
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+            if (t - t0 > kLimitNs) return false;
+        }
+    }
+}
+
 }  // namespace dg

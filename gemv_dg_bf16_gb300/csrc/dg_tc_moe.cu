@@ -49,33 +49,6 @@ struct TcMoeArgs {
     int stages;
 };
 
-// Sense-reversing grid barrier for a grid whose CTAs are all resident: counter at
-// bar[0], generation at bar[1] (in the workspace header; the last arriver resets
-// the counter for the next call).  Bounded: false after kWaitNs or
-// when this CTA already aborted.
-__device__ inline bool grid_barrier(unsigned* bar, volatile int* abort_flag)
-{
-    volatile unsigned* gen = bar + 1;
-    const unsigned my_gen = *gen;
-    if (atomicAdd(bar, 1u) == gridDim.x - 1) {
-        bar[0] = 0u;
-        __threadfence();
-        atomicAdd(bar + 1, 1u);
-        return true;
-    }
-    unsigned long long t0;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
-    for (uint32_t i = 1;; ++i) {
-        if (*gen != my_gen) return true;
-        if ((i & 63u) == 0) {
-            if (*abort_flag) return false;
-            unsigned long long t;
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-            if (t - t0 > kWaitNs) return false;
-        }
-    }
-}
-
 template <bool W1>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_moe_kernel(const __grid_constant__ CUtensorMap tmW, TcMoeArgs A)

@@ -28,7 +28,9 @@
  * - `ws` is a caller-owned device workspace of at least
  *   dg_workspace_bytes(op, ...) bytes.  It must be zero-filled once when it is
  *   allocated (e.g. cudaMemsetAsync); every call leaves its counters at zero
- *   again.  Calls that share one workspace must be ordered on one stream.
+ *   again (a grid barrier's generation word keeps counting; any value is fine).
+ *   Calls that share one workspace must be ordered on one stream.  After a
+ *   DG_DEVERR_WAIT_TIMEOUT the workspace must be zero-filled again.
  *   The first 16 bytes hold a sticky device status word (dg_device_status).
  * - `choice` may be NULL (dg_select picks); otherwise the given variant runs.
  * - Accumulation is fp32 in a fixed order that does not depend on the kernel
