@@ -147,7 +147,7 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
     // MoE: [1] warps per CTA, [3] N-tile (W1: gate/up columns, W2: output rows),
     // [4] pairs per pass -- the GB300 dg_sweep picks per row bucket.
     case DG_OP_MOE_W1:
-        if (M >= kTcMoeMinRows) {
+        if (M >= kTcMoeW1MinRows) {
             out->variant = DG_VAR_TC;
             break;
         }
@@ -157,7 +157,7 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
         out->params[4] = M <= 2 ? 4 : 2;
         break;
     case DG_OP_MOE_W2:
-        if (M >= kTcMoeMinRows) {
+        if (M >= kTcMoeW2MinRows) {
             out->variant = DG_VAR_TC;
             break;
         }

@@ -45,8 +45,11 @@ dg_status launch_tc_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, cons
 // Smallest row bucket the fp8 head sends to the tensor cores, and the largest K
 // whose split activations fit in shared memory.
 constexpr int kTcHeadMinRows = 2;
-// Smallest row bucket the MoE calls send to the tensor cores.
-constexpr int kTcMoeMinRows = 8;
+// Smallest row buckets the MoE calls send to the tensor cores (measured on GB300:
+// W2's grid-barrier combine makes its tensor-core kernel the faster one from 4
+// token rows, W1's from 8).
+constexpr int kTcMoeW1MinRows = 8;
+constexpr int kTcMoeW2MinRows = 4;
 constexpr int kTcHeadMaxK = 8192;
 
 struct DeviceInfo {

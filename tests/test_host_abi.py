@@ -88,8 +88,11 @@ def test_select_defaults_and_bucket_padding():
             c = dg.dg_select(op, M, 4096, 4096)
             dense_bf16 = op in (dg.DG_OP_GEMV_BF16, dg.DG_OP_GATE_UP_SILU)
             head = op == dg.DG_OP_HEAD_FP8_ARGMAX
-            moe = op in (dg.DG_OP_MOE_W1, dg.DG_OP_MOE_W2)
-            want = dg.DG_VAR_TC if (dense_bf16 and M >= 3) or (head and M >= 2) or (moe and M >= 7) else dg.DG_VAR_CC_WARP
+            w1 = op == dg.DG_OP_MOE_W1
+            w2 = op == dg.DG_OP_MOE_W2
+            # buckets: M=5 -> 6, M=7 -> 8
+            want = dg.DG_VAR_TC if ((dense_bf16 and M >= 3) or (head and M >= 2) or (w1 and M >= 7)
+                                    or (w2 and M >= 4)) else dg.DG_VAR_CC_WARP
             assert c.variant == want and c.from_table == 0, (op, M, c)
     with pytest.raises(dg.DGError):
         dg.dg_select(0, 129, 4096, 4096)
