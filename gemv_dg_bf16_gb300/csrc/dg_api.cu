@@ -436,7 +436,7 @@ extern "C" {
 dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int K, void* ws,
                        size_t ws_bytes, dg_stream_t stream, const dg_choice* choice)
 {
-    if (M < 1 || M > 128 || N < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxDenseRows || N < 1 || K < 1) return DG_ERR_INVALID_ARG;
     if (K % 8 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
     const void* ptrs[] = {x, W, y};
     dg_status s = check_common(ptrs, 3, ws, ws_bytes, dg_workspace_bytes(DG_OP_GEMV_BF16, M, N, K, 0));
@@ -462,7 +462,7 @@ dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int 
 dg_status dg_gate_up_silu(const void* x, const void* W_gu, void* out, int M, int N_half, int K,
                           void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice)
 {
-    if (M < 1 || M > 128 || N_half < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (M < 1 || M > kMaxDenseRows || N_half < 1 || K < 1) return DG_ERR_INVALID_ARG;
     if (K % 8 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
     const void* ptrs[] = {x, W_gu, out};
     dg_status s =

@@ -80,6 +80,9 @@ constexpr size_t kXsBudget = 96 * 1024;
 
 // Smallest row bucket the bf16 linear and gate/up send to the tensor cores.
 constexpr int kTcMinRows = 3;
+// Most token rows of one bf16 linear or gate/up call (the mid-M buckets 129..512 run
+// on the tensor cores in chunks of up to 256 tokens).
+constexpr int kMaxDenseRows = 512;
 
 // Compiled default choice for (op, M, N, K).
 void default_choice(dg_op op, int M, int N, int K, dg_choice* out);

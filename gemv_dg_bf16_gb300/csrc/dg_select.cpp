@@ -380,7 +380,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 6; }
+int dg_selection_space(void) { return 7; }
 
 const char* dg_build_id(void) { return build_id(); }
 

@@ -43,6 +43,7 @@ constexpr int kThreads = 192;
 constexpr int kMaxCluster = 8;                    // portable thread-block cluster size
 constexpr size_t kCoResidentSmem = 112 * 1024;    // two CTAs per SM
 constexpr int kPushMaxTokens = 8;                 // push fold up to this many tokens
+constexpr int kWideStages = 4;                    // 256-token tiles: 4 x 48 KB, one CTA per SM
 
 struct TcArgs {
     int N, K, M;
@@ -475,6 +476,8 @@ const void* tc_lookup(int mp, int epi)
     case 64 * 2 + 1: return tc_fn<64, 1>();
     case 128 * 2 + 0: return tc_fn<128, 0>();
     case 128 * 2 + 1: return tc_fn<128, 1>();
+    case 256 * 2 + 0: return tc_fn<256, 0>();
+    case 256 * 2 + 1: return tc_fn<256, 1>();
     default: return nullptr;
     }
 }
@@ -503,14 +506,15 @@ int default_stages(int mp, size_t recv)
 
 }  // namespace
 
-int tc_mp(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
+int tc_mp(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256))); }
 
 int tc_nsplit(int N, int K, int M)
 {
     const int tiles = (N + kTileRows - 1) / kTileRows;
     const int nkb = (K + kKB - 1) / kKB;
-    (void)M;
-    int ns = (160 + tiles - 1) / tiles;
+    // Up to 128 tokens two CTAs share an SM (about 160 CTAs in all); 256-token tiles
+    // take one SM each, so their split keeps the grid within one wave of 152.
+    int ns = tc_mp(M) <= 128 ? (160 + tiles - 1) / tiles : 152 / tiles;
     if (ns > kMaxCluster) ns = kMaxCluster;
     if (ns > nkb) ns = nkb;
     if (ns < 1) ns = 1;
@@ -529,8 +533,19 @@ size_t tc_workspace_bytes(int M, int N, int K)
 dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W,
                     void* out, int M, int N, int K, int ld_out, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
-    (void)dev;
-    if (M < 1 || M > 128) return DG_ERR_UNSUPPORTED_SHAPE;
+    if (M < 1 || M > kMaxDenseRows) return DG_ERR_UNSUPPORTED_SHAPE;
+    if (M > 256) {
+        // Mid-M: chunks of 256 token rows (the MMA's widest N), one launch each; the
+        // weights stream once per chunk.
+        for (int t0 = 0; t0 < M; t0 += 256) {
+            const int mc = M - t0 < 256 ? M - t0 : 256;
+            const dg_status st = launch_tc(gate_up, dev, c, static_cast<const uint16_t*>(x) + static_cast<size_t>(t0) * K,
+                                           W, static_cast<uint16_t*>(out) + static_cast<size_t>(t0) * ld_out, mc, N, K,
+                                           ld_out, ws, ws_bytes, stream);
+            if (st != DG_OK) return st;
+        }
+        return DG_OK;
+    }
     const int mp = tc_mp(M);
     const int epi = gate_up ? 1 : 0;
     const void* fn = tc_lookup(mp, epi);
@@ -542,8 +557,10 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
     // pulls the others' partials after a cluster barrier (measured on GB300: the
     // push is faster for few tokens, equal or slower beyond).  Same bits either way.
     size_t recv = mq <= kPushMaxTokens ? recv_bytes(ns, mq) : 0;
-    int stages = c.params[0] > 0 ? c.params[0] : default_stages(mp, 0);
+    int stages = c.params[0] > 0 ? c.params[0] : (mp <= 128 ? default_stages(mp, 0) : kWideStages);
     if (stages < 2 || stages > 8) return DG_ERR_BAD_VARIANT;
+    // The epilogue stages the tile (or parks the K-split partial) in the ring.
+    if (static_cast<size_t>(stages) * stage_bytes(mp) < static_cast<size_t>(mp) * kTileRows * 4) return DG_ERR_BAD_VARIANT;
     if (recv > 0 && smem_bytes(mp, stages, recv) > (c.params[0] > 0 ? kMaxDynSmem : kCoResidentSmem)) recv = 0;
     const size_t smem = smem_bytes(mp, stages, recv);
     if (smem > kMaxDynSmem) return DG_ERR_BAD_VARIANT;

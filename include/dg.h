@@ -2,7 +2,8 @@
  * dg.h -- libdecodegemm: decode-time skinny linear layers on GB300 (sm_103a).
  *
  * One C ABI for the five operations a decode step runs against large weight
- * matrices with few token rows (M = 1..128):
+ * matrices with few token rows (M = 1..128; the bf16 linear and gate/up also
+ * take the mid-M range 129..512):
  *
  *   dg_gemv_bf16        y = x . W^T, bf16 weights, bf16 out
  *   dg_gate_up_silu     out = silu(x . W_gate^T) * (x . W_up^T), one launch
@@ -172,7 +173,7 @@ dg_status dg_moe_route_debug(const int32_t* topk_ids, int M, int topk, int E, in
 
 /* Decode linear, mstar PR #1104 (decode GEMM table), "Why" / "What changed":
  *   y[m, n] = bf16_rn( sum_k x[m, k] * W[n, k] )   fp32 accumulation
- * x [M, K] bf16, W [N, K] bf16, y [M, N] bf16.  1 <= M <= 128. */
+ * x [M, K] bf16, W [N, K] bf16, y [M, N] bf16.  1 <= M <= 512. */
 dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int K,
                        void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice);
 
@@ -181,7 +182,7 @@ dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int 
  *   g = sum_k x[m,k] * W_gu[2j, k],  u = sum_k x[m,k] * W_gu[2j+1, k]   (fp32)
  *   out[m, j] = bf16_rn( silu(g) * u ),  silu(g) = g / (1 + exp(-g))     (fp32)
  * W_gu [2*N_half, K] bf16 stores gate row j at row 2j and up row j at 2j+1.
- * out [M, N_half] bf16.  1 <= M <= 128. */
+ * out [M, N_half] bf16.  1 <= M <= 512. */
 dg_status dg_gate_up_silu(const void* x, const void* W_gu, void* out, int M, int N_half, int K,
                           void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice);
 
@@ -248,7 +249,7 @@ dg_status dg_moe_w2(const void* a, const int32_t* topk_ids, const float* gw, con
 /* ---------------------------------------------------------------- selection */
 
 /* Kernel choice for (op, M, N, K): the loaded table's entry for M padded up to
- * the next row bucket (1 2 3 4 6 8 12 16 24 32 48 64 96 128), else the compiled
+ * the next row bucket (1 2 3 4 6 8 12 16 24 32 48 64 96 128 192 256 384 512), else the compiled
  * default for that bucket -- never a nearest-bucket guess.  mstar PR #1104
  * "What changed" (one per-device table; no table keeps the defaults);
  * "Decode optimization round 3", "Retained change 2" (padded-M lookup). */

@@ -238,3 +238,54 @@ def test_launch_without_pdl_gives_same_bits(cuda_device):
     y2 = dg.dg_gemv_bf16(y1, W, choice=CC)
     torch.cuda.synchronize()
     _lin_check(y1, W, y2)
+
+
+# ------------------------------------------------------------------ mid-M (129..512)
+
+MID_M = [129, 200, 256, 300, 512]
+
+
+@pytest.mark.parametrize("family", ["tc", "default"])
+@pytest.mark.parametrize("M,N,K", [(129, 300, 1040), (200, 640, 2056), (256, 257, 1096), (300, 130, 520),
+                                   (512, 384, 3080)])
+def test_gemv_mid_m_small(cuda_device, M, N, K, family):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K)
+    y = dg.dg_gemv_bf16(x, W, ws=ws, choice=FAMILIES[family])
+    torch.cuda.synchronize()
+    _lin_check(x, W, y)
+    assert dg.dg_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("N,K", [(32768, 1024), (8192, 1024), (4096, 12288)])
+@pytest.mark.parametrize("M", [192, 256, 512])
+def test_gemv_mid_m_full_size_sampled(cuda_device, M, N, K):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    y = dg.dg_gemv_bf16(x, W)
+    torch.cuda.synchronize()
+    _lin_check(x, W, y, rows=sample_rows(N, 48, seed=N + K + M))
+
+
+@pytest.mark.parametrize("M,N,K", [(200, 1000, 3080), (256, 4096, 4096)])
+def test_gemv_mid_m_tc_variants_bitwise_identical(cuda_device, M, N, K):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    ref = dg.dg_gemv_bf16(x, W, choice=TC)
+    for st in (2, 3, 4, 5, 8):
+        try:
+            y = dg.dg_gemv_bf16(x, W, choice=dg.Choice.make(dg.DG_VAR_TC, st))
+        except dg.DGError as e:            # a depth whose ring cannot hold the 256-token tile
+            assert e.status == 8, (st, e.status)
+            continue
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), st
+    # the CUDA-core family computes the same outputs within the tolerance
+    yc = dg.dg_gemv_bf16(x, W, choice=CC)
+    torch.cuda.synchronize()
+    _lin_check(x, W, yc, rows=sample_rows(N, 32, seed=M))
+
+
+@pytest.mark.parametrize("M", [160, 384])
+def test_gate_up_mid_m(cuda_device, M):
+    x, Wgu = S.gate_up_inputs(M, 700, 2056, device=cuda_device)
+    out = dg.dg_gate_up_silu(x, Wgu)
+    torch.cuda.synchronize()
+    _gate_up_check(x, Wgu, out)

@@ -55,7 +55,7 @@ def _gemv(x=A, W=A, y=A, M=2, N=64, K=256, ws=A, wsb=4096):
 
 def test_argument_errors_before_any_device_work():
     assert _gemv(M=0) == 1
-    assert _gemv(M=129) == 1
+    assert _gemv(M=513) == 1
     assert _gemv(K=250) == 3
     assert _gemv(x=0) == 1
     assert _gemv(W=U) == 2
@@ -94,8 +94,9 @@ def test_select_defaults_and_bucket_padding():
             want = dg.DG_VAR_TC if ((dense_bf16 and M >= 3) or (head and M >= 2) or (w1 and M >= 7)
                                     or (w2 and M >= 4)) else dg.DG_VAR_CC_WARP
             assert c.variant == want and c.from_table == 0, (op, M, c)
+    assert dg.dg_select(0, 129, 4096, 4096).variant == dg.DG_VAR_TC     # mid-M bucket 192
     with pytest.raises(dg.DGError):
-        dg.dg_select(0, 129, 4096, 4096)
+        dg.dg_select(0, 513, 4096, 4096)
     # a bucket's default does not depend on where in the bucket M falls
     assert dg.dg_select(0, 5, 64, 64).as_tuple() == dg.dg_select(0, 6, 64, 64).as_tuple()
 
