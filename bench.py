@@ -39,6 +39,8 @@ SWEEP_M = [1, 2, 4, 8, 16, 32, 64, 128]
 GATE_UP_M = [1, 2, 3, 4, 6, 8, 12, 16, 32, 64, 128]
 HEAD_M = [1, 2, 3, 4, 8]
 CHAIN_M = [1, 2, 4, 8, 16]
+MID_M = [192, 256, 384, 512]
+MID_NK = [(32768, 1024), (8192, 1024), (4096, 12288)]
 MOE_M = [1, 2, 4, 8, 16]
 MOE_E, MOE_I, MOE_K, MOE_TOPK = 128, 1536, 4096, 6
 HEAD_N, HEAD_K = 248320, 4096
@@ -260,6 +262,21 @@ def run_gpu(args):
                 [(lambda r=r, a=a, yv=yv, ws2=ws2, W2q=W2q, s2=s2: dg.dg_moe_w2(a, r[1], r[2], W2q, s2, yv, ws=ws2, stream=stream))
                  for r in routs], b2)
 
+        # --- mid-M bf16 linear (129..512 token rows) on three shapes
+        for (N, K) in MID_NK:
+            if not need("gemv_mid_m", [{"M": M, "N": N, "K": K} for M in MID_M]):
+                continue
+            W0 = S.linear_inputs(1, N, K, device=dev)[1]
+            wb = N * K * 2
+            Wm = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)]
+            for M in MID_M:
+                x = S.linear_inputs(M, N, K, device=dev)[0]
+                y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K, device=dev)
+                add("gemv_mid_m", {"M": M, "N": N, "K": K, "tflops_per_call": round(2 * M * N * K / 1e12, 6)},
+                    [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Wm], wb,
+                    launches_per_call=(M + 255) // 256)
+            del Wm
         # --- chained pairs inside one graph (PDL lets the second kernel's prologue and
         #     first weight loads overlap the first one's tail): MLP gate/up -> down
         #     projection, and MoE W1 -> W2
@@ -401,6 +418,8 @@ def run_gpu(args):
             continue
         s = summarize(i)
         ops.setdefault(s["op"], []).append(s)
+    for c in ops.get("gemv_mid_m", []):
+        c["tflops"] = round(c["tflops_per_call"] / (c["us"] * 1e-6), 1)
     # chained pairs: the same two calls measured on their own, for the PDL overlap
     sweep_by = {(s_["M"], s_["N"], s_["K"]): s_["us"] for s_ in sweep if "N" in s_}
     for c in ops.get("chain_mlp", []):
