@@ -3,7 +3,8 @@
 // CUDA-core FMA and bf16-unpack work per weight byte would start to bound it).
 //
 // Swap-AB: a CTA owns a tile of 128 weight rows (the MMA's M) and one fixed K
-// range; the tokens are the MMA's N (M padded to MP in {16, 32, 64, 128}), so
+// range; the tokens are the MMA's N (M padded to MP in {16, 32, 64, 128, 256};
+// calls of 257..512 rows run as chunks of 256), so
 // D[128, MP] = W_tile[128, Kr] . x[MP, Kr]^T accumulates in TMEM (fp32).
 //   warp 0      TMA producer: 128x64 weight box + MPx64 activation box per stage
 //               (128-byte swizzle), into a ring of `stages` shared-memory slots
@@ -11,7 +12,8 @@
 //               commits each stage back to its "empty" barrier and the last one
 //               to the accumulator barrier
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
-//               32*(w%4)..+31), then store / pair gate+up / write a K-split partial
+//               32*(w%4)..+31), stage the tile in the idle ring and write it out
+//               in coalesced pieces (store / pair gate+up), or fold a K-split
 // Canonical order of this family: the K range of a tile is cut into `nsplit`
 // contiguous ranges of 64-element blocks, a fixed function of (N, K, MP)
 // (tc_nsplit below); each range is one MMA chain from zero in ascending k; the
@@ -521,12 +523,12 @@ int tc_nsplit(int N, int K, int M)
     return ns;
 }
 
+// The K-split folds stay on chip, so only the status word is needed.
 size_t tc_workspace_bytes(int M, int N, int K)
 {
-    const int tiles = (N + kTileRows - 1) / kTileRows;
-    const int ns = tc_nsplit(N, K, M);
-    (void)tiles;
-    (void)ns;
+    (void)M;
+    (void)N;
+    (void)K;
     return kWsData;
 }
 
