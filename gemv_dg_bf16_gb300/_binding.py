@@ -93,6 +93,10 @@ def lib():
     L.dg_set_launch_flags.restype = S
     L.dg_launch_flags.argtypes = []
     L.dg_launch_flags.restype = ctypes.c_uint
+    L.dg_set_numerics.argtypes = [I]
+    L.dg_set_numerics.restype = S
+    L.dg_numerics.argtypes = []
+    L.dg_numerics.restype = I
     L.dg_gemv_bf16.argtypes = [P, P, P, I, I, I, P, Z, P, P]
     L.dg_gate_up_silu.argtypes = [P, P, P, I, I, I, P, Z, P, P]
     L.dg_head_fp8_argmax.argtypes = [P, P, P, P, P, I, I, I, P, Z, P, P]
@@ -163,6 +167,18 @@ def dg_set_launch_flags(flags: int):
 
 def dg_launch_flags() -> int:
     return int(lib().dg_launch_flags())
+
+
+DG_NUMERICS_FASTEST = 0
+DG_NUMERICS_BATCH_INVARIANT = 1
+
+
+def dg_set_numerics(mode: int):
+    _ok(lib().dg_set_numerics(int(mode)), "dg_set_numerics")
+
+
+def dg_numerics() -> int:
+    return int(lib().dg_numerics())
 
 
 def dg_selftest_wait_timeout(ws, timeout_us: int = 20000, stream=None):

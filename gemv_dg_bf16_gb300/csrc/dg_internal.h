@@ -26,7 +26,7 @@ const void* moe_w2_kernel(int mtmax);
 // tcgen05 family (dg_tc_dense.cu): padded token count, fixed K-split of a shape,
 // workspace bytes, and the launcher (bf16 linear or interleaved gate/up rows).
 int tc_mp(int M);
-int tc_nsplit(int N, int K, int M);
+int tc_nsplit(int N, int K, int M, bool fixed);
 size_t tc_workspace_bytes(int M, int N, int K);
 
 struct DeviceInfo;

@@ -10,6 +10,7 @@
 // the parser, the launchers and the sweep.
 // "Decode optimization round 3", "Retained change 2": lookups pad M up to the
 // next listed bucket and never fall back to a nearest row.
+#include <atomic>
 #include <cctype>
 #include <cstdio>
 #include <cstdlib>
@@ -186,7 +187,9 @@ std::string check_choice(int op, const dg_choice& c)
 {
     if (c.variant == DG_VAR_TC) {
         if (c.params[0] != 0 && (c.params[0] < 2 || c.params[0] > 8)) return "pipeline stages must be 2..8";
-        for (int i = 1; i < 6; ++i)
+        const bool dense = op == DG_OP_GEMV_BF16 || op == DG_OP_GATE_UP_SILU;
+        if (dense && c.params[1] != 0 && c.params[1] != 1) return "tensor-core K-split rule must be 0 or 1";
+        for (int i = dense ? 2 : 1; i < 6; ++i)
             if (c.params[i] != 0) return "unused tensor-core parameter set";
         return "";
     }
@@ -374,13 +377,39 @@ int bucket_rows(int M)
 
 const char* op_key_name(int op) { return op_name(op); }
 
+namespace {
+
+std::atomic<int> g_numerics{DG_NUMERICS_FASTEST};
+
+// The one family every bucket of `op` takes in the batch-invariant mode: the
+// tensor cores, except for an fp8 head too wide for their shared-memory split
+// activations, which stays on the CUDA cores at every row count.
+bool cuda_core_family(int variant) { return variant == DG_VAR_CC_WARP || variant == DG_VAR_CC_BULK; }
+
+int invariant_variant(int op, int K)
+{
+    if (op == DG_OP_HEAD_FP8_ARGMAX && K > kTcHeadMaxK) return DG_VAR_CC_WARP;
+    return DG_VAR_TC;
+}
+
+bool same_family(int a, int b) { return a == b || (cuda_core_family(a) && cuda_core_family(b)); }
+
+// The tensor-core linears cut K by a rule that depends on the row count beyond 128
+// rows; params[1] = 1 fixes it to the shape alone.
+void fix_split(int op, dg_choice* c)
+{
+    if (c->variant == DG_VAR_TC && (op == DG_OP_GEMV_BF16 || op == DG_OP_GATE_UP_SILU)) c->params[1] = 1;
+}
+
+}  // namespace
+
 }  // namespace dg
 
 using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 7; }
+int dg_selection_space(void) { return 8; }
 
 const char* dg_build_id(void) { return build_id(); }
 
@@ -451,16 +480,35 @@ dg_status dg_select(dg_op op, int M, int N, int K, dg_choice* out)
         }
         return DG_ERR_BAD_VARIANT;
     }
+    const bool invariant = g_numerics.load(std::memory_order_relaxed) == DG_NUMERICS_BATCH_INVARIANT;
+    const int fam = invariant_variant(op, K);
     {
         std::lock_guard<std::mutex> lk(g_tmu);
         auto it = g_table.find(Key(op, b, N, K));
-        if (it != g_table.end()) {
+        if (it != g_table.end() && (!invariant || same_family(it->second.choice.variant, fam))) {
             *out = it->second.choice;
+            if (invariant) fix_split(op, out);
             return DG_OK;
         }
     }
     default_choice(op, b, N, K, out);
+    if (invariant && !same_family(out->variant, fam)) {
+        // the family's own defaults: TC params are all derived from the shape, and a
+        // CUDA-core head bucket is never out of its family here
+        std::memset(out, 0, sizeof *out);
+        out->variant = fam;
+    }
+    if (invariant) fix_split(op, out);
     return DG_OK;
 }
+
+dg_status dg_set_numerics(int mode)
+{
+    if (mode != DG_NUMERICS_FASTEST && mode != DG_NUMERICS_BATCH_INVARIANT) return DG_ERR_INVALID_ARG;
+    g_numerics.store(mode);
+    return DG_OK;
+}
+
+int dg_numerics(void) { return g_numerics.load(); }
 
 }  // extern "C"

@@ -106,7 +106,11 @@ std::vector<dg_choice> candidates(int op, const dg_choice& def)
         out.push_back(c);
     };
     if (def.variant == DG_VAR_TC) {
-        for (int st = 2; st <= 8; ++st) add(mk(DG_VAR_TC, st));
+        for (int st = 2; st <= 8; ++st) {
+            dg_choice c = mk(DG_VAR_TC, st);
+            c.params[1] = def.params[1];       // the K-split rule is part of the arithmetic
+            add(c);
+        }
     } else if (op == DG_OP_MOE_W1 || op == DG_OP_MOE_W2) {
         const bool w1 = op == DG_OP_MOE_W1;
         for (int mt : {1, 2, 4})

@@ -15,8 +15,8 @@
 //               32*(w%4)..+31), stage the tile in the idle ring and write it out
 //               in coalesced pieces (store / pair gate+up), or fold a K-split
 // Canonical order of this family: the K range of a tile is cut into `nsplit`
-// contiguous ranges of 64-element blocks, a fixed function of (N, K, MP)
-// (tc_nsplit below); each range is one MMA chain from zero in ascending k; the
+// contiguous ranges of 64-element blocks, a fixed function of (N, K, MP), or of
+// (N, K) alone for the fixed split (tc_nsplit below); each range is one MMA chain from zero in ascending k; the
 // range partials are folded left in fp32.  The nsplit CTAs of a tile form one
 // thread-block cluster and each rank folds a slice of the tile's rows, over all
 // ranks in rank order.  Up to 8 tokens the ranks push their rows into the folding
@@ -510,13 +510,15 @@ int default_stages(int mp, size_t recv)
 
 int tc_mp(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256))); }
 
-int tc_nsplit(int N, int K, int M)
+int tc_nsplit(int N, int K, int M, bool fixed)
 {
     const int tiles = (N + kTileRows - 1) / kTileRows;
     const int nkb = (K + kKB - 1) / kKB;
     // Up to 128 tokens two CTAs share an SM (about 160 CTAs in all); 256-token tiles
-    // take one SM each, so their split keeps the grid within one wave of 152.
-    int ns = tc_mp(M) <= 128 ? (160 + tiles - 1) / tiles : 152 / tiles;
+    // take one SM each, so their split keeps the grid within one wave of 152.  A
+    // fixed split takes the first rule at every row count, so a row's bits do not
+    // depend on how many rows share the call.
+    int ns = (fixed || tc_mp(M) <= 128) ? (160 + tiles - 1) / tiles : 152 / tiles;
     if (ns > kMaxCluster) ns = kMaxCluster;
     if (ns > nkb) ns = nkb;
     if (ns < 1) ns = 1;
@@ -552,7 +554,8 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
     const int epi = gate_up ? 1 : 0;
     const void* fn = tc_lookup(mp, epi);
     if (!fn) return DG_ERR_BAD_VARIANT;
-    const int ns = tc_nsplit(N, K, M);
+    if (c.params[1] != 0 && c.params[1] != 1) return DG_ERR_BAD_VARIANT;
+    const int ns = tc_nsplit(N, K, M, c.params[1] == 1);
     const int mq = (M + 3) & ~3;
     // K-split fold: ranks push their rows to the folding rank (st.async) for up to 8
     // tokens when the receive buffer costs no pipeline stage; otherwise each rank

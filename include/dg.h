@@ -89,7 +89,10 @@ typedef enum {
  *                   sharing one row group's K segments (1, 2, 4, 8 dividing [1];
  *                   0 = 1) -- the segment partials are folded in the same order
  *   DG_VAR_CC_BULK: [0] 0, [1] pipeline stages (0 = as many as fit), [2] CTAs per SM (0 = 1)
- *   DG_VAR_TC:      [0] pipeline stages (0 = derived from the shape)
+ *   DG_VAR_TC:      [0] pipeline stages (0 = derived from the shape); bf16 linear and
+ *                   gate/up: [1] K-split rule, 0 = sized by the shape and the row
+ *                   count, 1 = by the shape alone (the batch-invariant mode's choice;
+ *                   the two agree up to 128 rows)
  * For the MoE ops, params[3] is the N-tile width in rows (0 = derived) and
  * params[4] the most (token, slot) pairs of one expert per pass over its rows
  * (1, 2, 4 or 8; 0 = 2). */
@@ -142,6 +145,27 @@ dg_status dg_device_status(const void* ws, int32_t* host_out, dg_stream_t stream
 #define DG_LAUNCH_PDL 0x1u
 dg_status dg_set_launch_flags(unsigned flags);
 unsigned dg_launch_flags(void);
+
+/* Numerics mode (process-wide); it steers dg_select, and so every call made with a
+ * NULL choice.
+ *   DG_NUMERICS_FASTEST (default): each row bucket takes its fastest kernel family.
+ *     The CUDA-core families (1-2 rows for the linears) and the tensor-core
+ *     families reduce in different orders, so a row's bits can change when the
+ *     same row is computed inside a larger batch (both meet the same error bound).
+ *   DG_NUMERICS_BATCH_INVARIANT: every bucket of an op takes one family (the
+ *     tensor cores; the fp8 head with K > 8192 the CUDA cores), so output row m is
+ *     a function of input row m alone -- for the MoE ops, of token m's activations,
+ *     ids and gate weights -- whatever M is and whatever the other rows hold.  A
+ *     one-row draft pass and a many-row verify pass then give the same logits and
+ *     the same argmax for the same row.  Table picks from another family are
+ *     ignored in this mode; an explicit choice passed to a call is used as given.
+ * The pages ask for bitwise-equal results per shape only (Strata PR #1297,
+ * "Summary"; "Decode optimization round 3", "Validation"); this mode extends the
+ * guarantee across row counts at the cost of the CUDA-core speed at 1-2 rows. */
+#define DG_NUMERICS_FASTEST 0
+#define DG_NUMERICS_BATCH_INVARIANT 1
+dg_status dg_set_numerics(int mode);   /* DG_ERR_INVALID_ARG for an unknown mode */
+int dg_numerics(void);
 
 /* Clear the device status word (asynchronous on `stream`). */
 dg_status dg_device_status_clear(void* ws, dg_stream_t stream);
@@ -196,6 +220,8 @@ dg_status dg_gate_up_silu(const void* x, const void* W_gu, void* out, int M, int
  *                 (a row of only NaN gives -1)
  * x [M, K] bf16, Wq [N, K] e4m3 codes, scale: device pointer to one fp32,
  * logits [M, N] bf16 or NULL, argmax [M] int32.  1 <= M <= 8.
+ * The CUDA-core kernels (one row, or K > 8192) stage every row's activations in
+ * shared memory: there M * K <= 49,152, else DG_ERR_UNSUPPORTED_SHAPE.
  * The argmax buffer is sized by this call's M. */
 dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, void* logits,
                              int32_t* argmax, int M, int N, int K, void* ws, size_t ws_bytes,

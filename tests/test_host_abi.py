@@ -207,3 +207,39 @@ def test_binding_constants_match_header():
     assert len(enums) == 9 and len(defines) == 2
     for name, val in {**enums, **defines}.items():
         assert getattr(dg, name) == val, name
+
+
+def test_batch_invariant_numerics_takes_one_family_per_op():
+    assert dg.dg_numerics() == dg.DG_NUMERICS_FASTEST
+    with pytest.raises(dg.DGError):
+        dg.dg_set_numerics(2)
+    # the fastest mode mixes families across row buckets
+    assert dg.dg_select(dg.DG_OP_GEMV_BF16, 1, 4096, 4096).variant == dg.DG_VAR_CC_WARP
+    assert dg.dg_select(dg.DG_OP_GEMV_BF16, 8, 4096, 4096).variant == dg.DG_VAR_TC
+    dg.dg_set_numerics(dg.DG_NUMERICS_BATCH_INVARIANT)
+    try:
+        assert dg.dg_numerics() == dg.DG_NUMERICS_BATCH_INVARIANT
+        top = {dg.DG_OP_GEMV_BF16: 512, dg.DG_OP_GATE_UP_SILU: 512, dg.DG_OP_HEAD_FP8_ARGMAX: 8,
+               dg.DG_OP_MOE_W1: 16, dg.DG_OP_MOE_W2: 16}
+        for op, mmax in top.items():
+            picks = {dg.dg_select(op, M, 4096, 4096).as_tuple() for M in range(1, mmax + 1)}
+            assert {p[0] for p in picks} == {dg.DG_VAR_TC}, (op, picks)
+            dense = op in (dg.DG_OP_GEMV_BF16, dg.DG_OP_GATE_UP_SILU)
+            # the tensor-core linears take the K-split fixed by the shape alone
+            assert {p[1][1] for p in picks} == ({1} if dense else {0}), (op, picks)
+        # a head too wide for the tensor-core split stays on the CUDA cores at every M
+        assert {dg.dg_select(dg.DG_OP_HEAD_FP8_ARGMAX, M, 248320, 16384).variant for M in range(1, 9)} == \
+            {dg.DG_VAR_CC_WARP}
+    finally:
+        dg.dg_set_numerics(dg.DG_NUMERICS_FASTEST)
+    assert dg.dg_select(dg.DG_OP_GEMV_BF16, 1, 4096, 4096).variant == dg.DG_VAR_CC_WARP
+    assert dg.dg_select(dg.DG_OP_GEMV_BF16, 300, 4096, 4096).params[1] == 0
+
+
+def test_tc_split_rule_parameter_checked(tmp_path):
+    ent = lambda op, p: [{"op": op, "M": 4, "N": 64, "K": 64, "pick": {"variant": 3, "params": p}}]
+    assert _check(_table(tmp_path, entries=ent("gemv_bf16", [0, 1])))[0] == 0
+    s, _, why = _check(_table(tmp_path, entries=ent("gemv_bf16", [0, 2])))
+    assert s == 6 and "K-split rule" in why
+    s, _, why = _check(_table(tmp_path, entries=ent("moe_w1_silu", [0, 1])))
+    assert s == 6 and "unused tensor-core parameter" in why
