@@ -364,3 +364,106 @@ DGO_API void dgo_moe_w2(const uint16_t* a, const int32_t* ids, const float* gw, 
                 absdot[t * Nout + n] = bound;
         }
 }
+
+/* ---------------------------------------------------------------- A8W8 blockscale
+ * The A8W8 block-scaled linear and the activation quantisation it takes as a
+ * prologue ("Decode optimization round 3", "Retained change 2: decode-M rows for
+ * the A8W8 bpreshuffle table", and "Rejected paths" / "Remaining headroom": the
+ * quantisation kernels fused into the GEMM).  Blocks are 128 wide along K: one
+ * activation scale per (token, K-block), one weight scale per 128 x 128 block.
+ * The pages give no formulas; the quantisation below is the plain per-block
+ * max-scaling to the e4m3 range, decided in binary32. */
+
+/* Nearest e4m3 code to a binary32 value, ties to even, magnitudes beyond 448
+ * clamped to 448 (saturating), NaN to 0x7F.  Written from the field layout:
+ * normal values (1 + m/8) * 2^(e-7) for biased exponent e = 1..15, subnormals
+ * m * 2^-9. */
+DGO_API uint8_t dgo_e4m3_encode(float v)
+{
+    if (isnan(v))
+        return 0x7F;
+    const uint8_t sign = signbit(v) ? 0x80 : 0;
+    double a = fabs((double)v);
+    if (a >= 448.0)
+        return sign | 0x7E;
+    if (a < 0x1p-6) {                                   /* subnormal range, spacing 2^-9 */
+        const double m = nearbyint(a * 0x1p9);         /* 0 .. 8; 8 is the smallest normal */
+        return sign | (uint8_t)m;
+    }
+    int e;
+    frexp(a, &e);                                       /* a = f * 2^e, f in [0.5, 1) */
+    const int unbiased = e - 1;                         /* a = (1 + m/8) * 2^unbiased */
+    double m = nearbyint(ldexp(a, 3 - unbiased)) - 8.0; /* 0 .. 8 */
+    int ub = unbiased;
+    if (m >= 8.0) {
+        m = 0.0;
+        ++ub;
+    }
+    if (ub + 7 > 15 || (ub + 7 == 15 && m > 6.0))     /* above 448 after rounding */
+        return sign | 0x7E;
+    return sign | (uint8_t)(((ub + 7) << 3) | (int)m);
+}
+
+/* Per token m and K-block b (elements b*128 .. min(K, b*128+128) - 1), in binary32:
+ *   amax = max(max |x|, 2^-32)      (all-zero blocks quantise to zero codes)
+ *   r    = 448 / amax               sx[m, b] = amax / 448
+ *   q[m, k] = e4m3(x[m, k] * r)
+ * x [M, K] bf16 bits; q [M, K] codes; sx [M, ceil(K/128)]. */
+DGO_API void dgo_a8_quant(const uint16_t* x, int64_t M, int64_t K, uint8_t* q, float* sx)
+{
+    const int64_t nb = (K + 127) / 128;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < nb; ++b) {
+            const int64_t k0 = b * 128, k1 = k0 + 128 < K ? k0 + 128 : K;
+            float amax = 0.0f;
+            for (int64_t k = k0; k < k1; ++k) {
+                const float a = fabsf((float)bf16_value(x[m * K + k]));
+                if (a > amax)
+                    amax = a;
+            }
+            if (amax < 0x1p-32f)
+                amax = 0x1p-32f;
+            const float r = 448.0f / amax;
+            sx[m * nb + b] = amax / 448.0f;
+            for (int64_t k = k0; k < k1; ++k) {
+                const float v = (float)bf16_value(x[m * K + k]) * r;
+                q[m * K + k] = dgo_e4m3_encode(v);
+            }
+        }
+}
+
+/* y[m, r] = sum over K-blocks b of sx[m,b] * sw[n/128, b] * sum_{k in b} e4m3(q[m,k]) *
+ * e4m3(Wq[n,k]) for the requested rows n = n_r, in double (every product and the
+ * block sums are exact there; the blocks are added in ascending b).
+ * absdot[m, r] = sum_b |sx * sw| * sum_k |q * w|.  Wq [N, K] codes,
+ * sw [ceil(N/128), ceil(K/128)] fp32 row-major. */
+DGO_API void dgo_a8w8_linear(const uint8_t* q, const float* sx, const uint8_t* Wq, const float* sw,
+                             int64_t M, int64_t K, const int64_t* rows, int64_t nrows, double* y,
+                             double* absdot)
+{
+    e4m3_table_init();
+    const int64_t nb = (K + 127) / 128;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t n = pick_row(rows, r);
+        const uint8_t* w = Wq + n * K;
+        for (int64_t m = 0; m < M; ++m) {
+            double s = 0.0, a = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const int64_t k0 = b * 128, k1 = k0 + 128 < K ? k0 + 128 : K;
+                double d = 0.0, ad = 0.0;
+                for (int64_t k = k0; k < k1; ++k) {
+                    const double p = E4M3(q[m * K + k]) * E4M3(w[k]);
+                    d += p;
+                    ad += fabs(p);
+                }
+                const double c = (double)sx[m * nb + b] * (double)sw[(n / 128) * nb + b];
+                s += c * d;
+                a += fabs(c) * ad;
+            }
+            y[m * nrows + r] = s;
+            if (absdot)
+                absdot[m * nrows + r] = a;
+        }
+    }
+}

@@ -52,6 +52,10 @@ def lib():
         L.dgo_moe_route.restype = ctypes.c_int32
         L.dgo_moe_w1_silu.argtypes = [P, P, P, P, I64, I64, I64, I64, I64, P, P, P, P, P]
         L.dgo_moe_w2.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I64, P, P]
+        L.dgo_e4m3_encode.argtypes = [ctypes.c_float]
+        L.dgo_e4m3_encode.restype = ctypes.c_uint8
+        L.dgo_a8_quant.argtypes = [P, I64, I64, P, P]
+        L.dgo_a8w8_linear.argtypes = [P, P, P, P, I64, I64, P, I64, P, P]
         _lib = L
     return _lib
 
@@ -183,3 +187,40 @@ def moe_w2(a, ids, gw, W2q, s2):
     lib().dgo_moe_w2(pa, pi, pg, pW, ps, M, topk, E, I, Nout, y.ctypes.data_as(ctypes.c_void_p),
                      b.ctypes.data_as(ctypes.c_void_p))
     return y, b
+
+
+def e4m3_encode(v: float) -> int:
+    """Nearest e4m3 code (ties to even, saturating at 448) of a binary32 value."""
+    return int(lib().dgo_e4m3_encode(float(v)))
+
+
+def a8_quant(x):
+    """x [M,K] uint16 bf16 bits -> (q [M,K] uint8 e4m3 codes, sx [M, ceil(K/128)] float32)."""
+    x, px = _c(x, np.uint16)
+    M, K = x.shape
+    q = np.empty((M, K), np.uint8)
+    sx = np.empty((M, (K + 127) // 128), np.float32)
+    lib().dgo_a8_quant(px, M, K, q.ctypes.data_as(ctypes.c_void_p), sx.ctypes.data_as(ctypes.c_void_p))
+    return q, sx
+
+
+def a8w8_linear_q(q, sx, Wq, sw, rows=None):
+    """Block-scaled product of quantised activations: -> (y [M,nrows] f64, absdot [M,nrows] f64)."""
+    q, pq = _c(q, np.uint8)
+    sx, psx = _c(sx, np.float32)
+    Wq, pW = _c(Wq, np.uint8)
+    sw, psw = _c(sw, np.float32)
+    M, K = q.shape
+    _r, pr, nr = _rows(rows, Wq.shape[0])
+    y = np.empty((M, nr)); a = np.empty((M, nr))
+    lib().dgo_a8w8_linear(pq, psx, pW, psw, M, K, pr, nr, y.ctypes.data_as(ctypes.c_void_p),
+                          a.ctypes.data_as(ctypes.c_void_p))
+    return y, a
+
+
+def a8w8_linear(x, Wq, sw, rows=None):
+    """The whole A8W8 step on bf16 activations: quantise, then the block-scaled product.
+    -> dict(y, absdot, q, sx)."""
+    q, sx = a8_quant(x)
+    y, a = a8w8_linear_q(q, sx, Wq, sw, rows)
+    return {"y": y, "absdot": a, "q": q, "sx": sx}

@@ -14,6 +14,8 @@ Recipes (the distributions the workloads are specified with):
     ``topk`` scores ~ N(0,1) turned into gate weights by a softmax (fp64, stored fp32);
     W1 [E, 2I, K] and W2 [E, Nout, I] ~ N(0, 1/K_in) quantised to e4m3 with one fp32
     scale per output row (max over that row / 448).
+  * A8W8 blockscale linear: x ~ N(0,1) bf16 [M,K]; W ~ N(0,1/K) [N,K] quantised to e4m3
+    with one fp32 scale per 128 x 128 block (max over the block / 448).
 
 Quantisation here is input preparation (it produces the bytes the kernels read);
 it uses torch's own float8_e4m3fn cast after clamping to the finite range.
@@ -29,6 +31,7 @@ E4M3_MAX = 448.0
 __all__ = [
     "seed_for", "normal_bf16", "linear_inputs", "gate_up_inputs", "quantize_e4m3_per_tensor",
     "quantize_e4m3_per_row", "head_inputs", "moe_routing", "moe_weights", "moe_inputs", "E4M3_MAX",
+    "quantize_e4m3_blocks", "a8w8_inputs",
 ]
 
 
@@ -140,3 +143,33 @@ def moe_inputs(M: int, K: int, topk: int, E: int, rep: int = 0, device="cpu"):
     x = normal_bf16((M, K), 1.0, seed_for("moe_x", M, K, rep), device)
     ids, w = moe_routing(M, topk, E, seed_for("moe_route", M, topk, E, rep))
     return x, ids.to(device), w.to(device)
+
+
+def quantize_e4m3_blocks(w: torch.Tensor, block: int = 128):
+    """fp32 [N, K] -> (uint8 e4m3 codes [N, K], fp32 scales [ceil(N/128), ceil(K/128)]);
+    one scale per 128 x 128 block, max|w|/448 of the block (1 for an all-zero block)."""
+    N, K = w.shape
+    nbn, nbk = (N + block - 1) // block, (K + block - 1) // block
+    pad = torch.zeros((nbn * block, nbk * block), dtype=torch.float32, device=w.device)
+    pad[:N, :K] = w
+    blocks = pad.view(nbn, block, nbk, block)
+    amax = blocks.abs().amax(dim=(1, 3))
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = _to_e4m3_bytes(blocks / scale[:, None, :, None]).view(nbn * block, nbk * block)[:N, :K].contiguous()
+    return q, scale.contiguous()
+
+
+def a8w8_inputs(M: int, N: int, K: int, device="cpu", chunk_rows: int = 8192):
+    """x [M,K] bf16 ~ N(0,1); Wq [N,K] e4m3 codes and sw [ceil(N/128), ceil(K/128)] fp32 from
+    W ~ N(0, 1/K) quantised per 128 x 128 block (row chunks of 128 rows keep memory bounded)."""
+    seedW = seed_for("a8w8", "W", N, K)
+    Wq = torch.empty((N, K), dtype=torch.uint8, device=device)
+    sw = torch.empty(((N + 127) // 128, (K + 127) // 128), dtype=torch.float32, device=device)
+    for r0 in range(0, N, chunk_rows):
+        r1 = min(N, r0 + chunk_rows)
+        w = torch.randn((r1 - r0, K), generator=_gen(seedW + r0, device), device=device) * K ** -0.5
+        q, s = quantize_e4m3_blocks(w)
+        Wq[r0:r1] = q
+        sw[r0 // 128:(r1 + 127) // 128] = s
+    x = normal_bf16((M, K), 1.0, seed_for("a8w8", "x", N, K, M), device)
+    return x, Wq, sw

@@ -366,3 +366,187 @@ def test_moe_w2_brute_force_and_reductions():
     ys, _ = O.moe_w2(a_same, ids.numpy(), gw_eq, W2same, s2same)
     single = np.stack([(af[t, 0] @ w2[0].T) * s2n[0] for t in range(M)])
     assert np.allclose(ys, single * topk / 4, rtol=1e-13)
+
+
+# ---------------------------------------------------------------- A8W8 blockscale
+
+def _e4m3_encode_lib(v32: np.ndarray) -> np.ndarray:
+    """binary32 values -> e4m3 codes by torch's own float8_e4m3fn cast (round to nearest
+    even), after clamping to +-448 (the saturating conversion)."""
+    t = torch.from_numpy(np.asarray(v32, np.float32)).clamp(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_encode_hand_worked_points():
+    with open(os.path.join(GOLDEN, "e4m3_rne_points.txt")) as f:
+        rows = [ln.split()[:2] for ln in f if ln.strip() and not ln.startswith("#")]
+    assert len(rows) >= 12
+    for val, code in rows:
+        assert O.e4m3_encode(float(Fraction(val))) == int(code, 16), (val, code)
+
+
+def test_e4m3_encode_matches_library_rounding():
+    finite = [c for c in range(0x7F)]
+    vals = [O.e4m3_value(c) for c in finite]
+    mids = [(a + b) / 2 for a, b in zip(vals, vals[1:])]                 # exact ties
+    g = np.random.default_rng(11)
+    rnd = (g.standard_normal(20000) * np.exp2(g.uniform(-12, 10, 20000))).astype(np.float32)
+    pts = np.concatenate([np.float32(vals), np.float32(mids), np.nextafter(np.float32(mids), np.float32(0)),
+                          np.nextafter(np.float32(mids), np.float32(1e9)), rnd, -rnd[:2000]]).astype(np.float32)
+    lib = _e4m3_encode_lib(pts)
+    got = np.array([O.e4m3_encode(float(v)) for v in pts], np.uint8)
+    assert np.array_equal(got, lib), pts[got != lib][:8]
+    # every finite code round-trips
+    for c in list(range(0x7F)) + list(range(0x80, 0xFF)):
+        assert O.e4m3_encode(O.e4m3_value(c)) == (c if c != 0x80 else 0x80), hex(c)
+
+
+def _quant_numpy(xbits: np.ndarray):
+    """Per (token, 128-block) quantisation written with numpy binary32 arithmetic and
+    torch's e4m3 cast (independent of the oracle's C code)."""
+    x = bf16_float(xbits).astype(np.float32)
+    M, K = x.shape
+    nb = (K + 127) // 128
+    q = np.zeros((M, K), np.uint8)
+    sx = np.zeros((M, nb), np.float32)
+    for m in range(M):
+        for b in range(nb):
+            blk = x[m, b * 128:(b + 1) * 128]
+            amax = np.float32(np.max(np.abs(blk)))
+            amax = max(amax, np.float32(2.0 ** -32))
+            r = np.float32(448.0) / amax
+            sx[m, b] = amax / np.float32(448.0)
+            q[m, b * 128:(b + 1) * 128] = _e4m3_encode_lib(blk * r)
+    return q, sx
+
+
+def _a8_inputs(M, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((M, K), generator=g)
+    nb = (K + 127) // 128
+    x *= torch.exp2(torch.randint(-20, 12, (M, nb), generator=g).float()).repeat_interleave(128, 1)[:, :K]
+    x[0, 128:256] = 0.0                                  # an all-zero block
+    if K > 300:
+        x[-1, 300] = 3.0e4                               # a spike that owns its block's scale
+    return bf16_bits(x.to(torch.bfloat16))
+
+
+@pytest.mark.parametrize("M,K,seed", [(3, 272, 1), (2, 1040, 2), (5, 128, 3)])
+def test_a8_quant_matches_independent_binary32(M, K, seed):
+    xb = _a8_inputs(M, K, seed)
+    q, sx = O.a8_quant(xb)
+    q_ref, sx_ref = _quant_numpy(xb)
+    assert np.array_equal(q, q_ref)
+    assert np.array_equal(sx.view(np.uint32), sx_ref.view(np.uint32))
+    if K >= 256:
+        assert (q[0, 128:256] == 0).all() and sx[0, 1] == np.float32(2.0 ** -32) / np.float32(448.0)
+    # every block that is not all zero has its largest magnitude on the top code, 448
+    qv = np.abs(e4m3_float_lib(q))
+    for m in range(M):
+        for b in range((K + 127) // 128):
+            blk = qv[m, b * 128:(b + 1) * 128]
+            assert blk.max() in (0.0, 448.0), (m, b, blk.max())
+
+
+def _a8w8_exact(q, sx, Wq, sw, K):
+    M, N = q.shape[0], Wq.shape[0]
+    nb = (K + 127) // 128
+    qv = e4m3_float_lib(q)
+    wv = e4m3_float_lib(Wq)
+    y = np.empty((M, N), object)
+    ad = np.empty((M, N), object)
+    for m in range(M):
+        for n in range(N):
+            s = Fraction(0)
+            a = Fraction(0)
+            for b in range(nb):
+                c = frac(sx[m, b]) * frac(sw[n // 128, b])
+                d = sum((frac(qv[m, k]) * frac(wv[n, k]) for k in range(b * 128, min(K, b * 128 + 128))), Fraction(0))
+                da = sum((abs(frac(qv[m, k]) * frac(wv[n, k])) for k in range(b * 128, min(K, b * 128 + 128))),
+                         Fraction(0))
+                s += c * d
+                a += abs(c) * da
+            y[m, n] = s
+            ad[m, n] = a
+    return y, ad
+
+
+def _a8w8_weights(N, K, seed):
+    g = torch.Generator().manual_seed(seed)
+    Wq = (torch.randn((N, K), generator=g) * 60).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    nbn, nbk = (N + 127) // 128, (K + 127) // 128
+    sw = (torch.rand((nbn, nbk), generator=g) * 1e-3 + 1e-4).numpy().astype(np.float32)
+    return Wq, sw
+
+
+def test_a8w8_linear_brute_force_exact():
+    """N = 130 puts rows 128..129 in the second weight-scale row; K = 272 makes three
+    K-blocks, the last one short: a wrong block index or a transposed scale fails."""
+    M, N, K = 2, 130, 272
+    xb = _a8_inputs(M, K, 5)
+    q, sx = O.a8_quant(xb)
+    Wq, sw = _a8w8_weights(N, K, 6)
+    rows = np.array([0, 1, 63, 127, 128, 129])
+    y, ad = O.a8w8_linear_q(q, sx, Wq, sw, rows=rows)
+    # exact sums, each row with its own weight-scale row n // 128
+    ye = np.empty((M, len(rows)), object)
+    ae = np.empty((M, len(rows)), object)
+    for j, n in enumerate(rows):
+        sw_row = np.zeros_like(sw)
+        sw_row[0] = sw[n // 128]
+        yy, aa = _a8w8_exact(q, sx, Wq[n:n + 1], sw_row, K)
+        ye[:, j], ae[:, j] = yy[:, 0], aa[:, 0]
+    for m in range(M):
+        for j in range(len(rows)):
+            tol = 1e-13 * float(ae[m, j]) + 1e-300
+            assert abs(y[m, j] - float(ye[m, j])) <= tol, (m, j)
+            assert abs(ad[m, j] - float(ae[m, j])) <= tol
+
+
+def test_a8w8_one_hot_closed_form():
+    """x = v e_k: the token's block holds one nonzero, which quantises to +-448, so
+    y[n] = sx * sw[n/128, k/128] * 448 * e4m3(W[n, k]) * sign(v)."""
+    M, N, K = 1, 260, 384
+    Wq, sw = _a8w8_weights(N, K, 8)
+    for k, v in [(5, 3.25), (200, -0.0078125), (383, 1.5e3)]:
+        x = torch.zeros((M, K))
+        x[0, k] = v
+        xb = bf16_bits(x.to(torch.bfloat16))
+        r = O.a8w8_linear(xb, Wq, sw)
+        q = r["q"]
+        assert q[0, k] == (0x7E if v > 0 else 0xFE) and np.count_nonzero(q) == 1
+        amax = np.float32(abs(np.float32(bf16_float(xb)[0, k])))
+        sxv = float(amax / np.float32(448.0))
+        assert r["sx"][0, k // 128] == np.float32(sxv)
+        w = e4m3_float_lib(Wq[:, k])
+        want = sxv * sw[np.arange(N) // 128, k // 128].astype(np.float64) * 448.0 * w * np.sign(v)
+        assert np.allclose(r["y"][0], want, rtol=1e-15, atol=0)
+
+
+def test_a8w8_reduces_to_head_when_scales_are_one():
+    """Blocks whose largest magnitude is exactly 448 and whose values are e4m3 numbers
+    quantise to themselves with sx = 1; with one weight scale c everywhere the step is
+    the fp8 head with scale c."""
+    M, N, K = 3, 140, 384
+    g = torch.Generator().manual_seed(9)
+    xv = (torch.randn((M, K), generator=g) * 50).clamp(-440, 440).to(torch.float8_e4m3fn).to(torch.float32)
+    xv[:, ::128] = 448.0                                 # every block's max is 448
+    xb = bf16_bits(xv.to(torch.bfloat16))
+    Wq, _ = _a8w8_weights(N, K, 10)
+    c = np.float32(0.0078125)
+    sw = np.full(((N + 127) // 128, K // 128), c, np.float32)
+    r = O.a8w8_linear(xb, Wq, sw)
+    assert (r["sx"] == 1.0).all()
+    assert np.array_equal(e4m3_float_lib(r["q"]), bf16_float(xb))
+    lg, ad = O.head_fp8(xb, Wq, float(c))
+    assert np.allclose(r["y"], lg, rtol=1e-14, atol=1e-300)
+    assert np.allclose(r["absdot"], ad, rtol=1e-14, atol=1e-300)
+
+
+def test_a8w8_weight_scale_is_linear_exactly():
+    M, N, K = 2, 200, 256
+    xb = _a8_inputs(M, K, 12)
+    Wq, sw = _a8w8_weights(N, K, 13)
+    y1 = O.a8w8_linear(xb, Wq, sw)["y"]
+    y2 = O.a8w8_linear(xb, Wq, (sw * np.float32(2.0)).astype(np.float32))["y"]
+    assert np.array_equal(y2, 2.0 * y1)
