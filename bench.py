@@ -42,6 +42,9 @@ CHAIN_M = [1, 2, 4, 8, 16]
 MID_M = [192, 256, 384, 512]
 MID_NK = [(32768, 1024), (8192, 1024), (4096, 12288)]
 MOE_M = [1, 2, 4, 8, 16]
+A8_NK = [(32768, 1024), (8192, 4096)]
+A8_M = [1, 2, 4, 8, 16, 32, 64]
+INV_M = [1, 2]
 MOE_E, MOE_I, MOE_K, MOE_TOPK = 128, 1536, 4096, 6
 HEAD_N, HEAD_K = 248320, 4096
 FALLBACK_HBM_GBS = 6800.0
@@ -277,6 +280,40 @@ def run_gpu(args):
                     [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Wm], wb,
                     launches_per_call=(M + 255) // 256)
             del Wm
+        # --- A8W8 block-scaled linear with the activation quantisation fused in
+        for (N, K) in A8_NK:
+            if not need("gemv_a8w8", [{"M": M, "N": N, "K": K} for M in A8_M]):
+                continue
+            _, Wq0, sw = S.a8w8_inputs(1, N, K, device=dev)
+            wb = N * K + sw.numel() * 4
+            Wa = [Wq0] + [Wq0.clone() for _ in range(_copies_for(wb, l2) - 1)]
+            for M in A8_M:
+                x = S.normal_bf16((M, K), 1.0, S.seed_for("a8w8", "x", N, K, M), dev)
+                y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                ws = dg.workspace(dg.DG_OP_GEMV_A8W8, M, N, K, device=dev)
+                add("gemv_a8w8", {"M": M, "N": N, "K": K},
+                    [(lambda W=W, x=x, y=y, ws=ws, sw=sw: dg.dg_gemv_a8w8_blockscale(x, W, sw, y, ws=ws, stream=stream))
+                     for W in Wa], wb)
+            del Wa
+        # --- the bf16 sweep shapes at 1-2 rows in the batch-invariant numerics mode (the
+        #     tensor-core family where the fastest mode takes the CUDA cores)
+        if need("gemv_bf16_invariant", [{"M": M, "N": N, "K": K} for (N, K) in SWEEP_NK for M in INV_M]):
+            dg.dg_set_numerics(dg.DG_NUMERICS_BATCH_INVARIANT)
+            try:
+                for (N, K) in SWEEP_NK:
+                    W0 = S.linear_inputs(1, N, K, device=dev)[1]
+                    wb = N * K * 2
+                    Wi = [W0] + [W0.clone() for _ in range(_copies_for(wb, l2) - 1)]
+                    for M in INV_M:
+                        x = S.linear_inputs(M, N, K, device=dev)[0]
+                        y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+                        ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K, device=dev)
+                        add("gemv_bf16_invariant", {"M": M, "N": N, "K": K},
+                            [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Wi],
+                            wb)
+                    del Wi
+            finally:
+                dg.dg_set_numerics(dg.DG_NUMERICS_FASTEST)
         # --- chained pairs inside one graph (PDL lets the second kernel's prologue and
         #     first weight loads overlap the first one's tail): MLP gate/up -> down
         #     projection, and MoE W1 -> W2
@@ -420,6 +457,9 @@ def run_gpu(args):
         ops.setdefault(s["op"], []).append(s)
     for c in ops.get("gemv_mid_m", []):
         c["tflops"] = round(c["tflops_per_call"] / (c["us"] * 1e-6), 1)
+    sweep_us = {(s_["M"], s_["N"], s_["K"]): s_["us"] for s_ in sweep if "N" in s_}
+    for c in ops.get("gemv_bf16_invariant", []):
+        c["fastest_mode_us"] = sweep_us.get((c["M"], c["N"], c["K"]))
     # chained pairs: the same two calls measured on their own, for the PDL overlap
     sweep_by = {(s_["M"], s_["N"], s_["K"]): s_["us"] for s_ in sweep if "N" in s_}
     for c in ops.get("chain_mlp", []):

@@ -15,7 +15,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIBPATH = os.path.join(_HERE, "libdecodegemm.so")
 
-DG_OP_GEMV_BF16, DG_OP_GATE_UP_SILU, DG_OP_HEAD_FP8_ARGMAX, DG_OP_MOE_W1, DG_OP_MOE_W2 = range(5)
+DG_OP_GEMV_BF16, DG_OP_GATE_UP_SILU, DG_OP_HEAD_FP8_ARGMAX, DG_OP_MOE_W1, DG_OP_MOE_W2, DG_OP_GEMV_A8W8 = range(6)
 DG_VAR_DEFAULT, DG_VAR_CC_WARP, DG_VAR_CC_BULK, DG_VAR_TC = range(4)
 (DG_OK, DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_UNSUPPORTED_SHAPE, DG_ERR_WORKSPACE_TOO_SMALL, DG_ERR_CUDA,
  DG_ERR_TABLE_REFUSED, DG_ERR_NO_DEVICE, DG_ERR_BAD_VARIANT) = range(9)
@@ -103,6 +103,8 @@ def lib():
     L.dg_head_fp8_argmax_noalloc.argtypes = [P, P, P, P, P, I, I, I, P, P]
     L.dg_moe_w1_silu.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
     L.dg_moe_w2.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
+    L.dg_gemv_a8w8_blockscale.argtypes = [P, P, P, P, I, I, I, P, Z, P, P]
+    L.dg_quant_a8_blockscale.argtypes = [P, P, P, I, I, P]
     L.dg_select.argtypes = [I, I, I, I, ctypes.POINTER(Choice)]
     L.dg_table_load.argtypes = [ctypes.c_char_p]
     L.dg_table_clear.argtypes = []
@@ -116,6 +118,7 @@ def lib():
     L.dg_sweep.argtypes = [ctypes.POINTER(Shape), I, ctypes.c_char_p, I]
     for name in ("dg_init", "dg_device_status", "dg_device_status_clear", "dg_gemv_bf16",
                  "dg_gate_up_silu", "dg_head_fp8_argmax", "dg_head_fp8_argmax_noalloc", "dg_moe_w1_silu", "dg_moe_w2", "dg_select",
+                 "dg_gemv_a8w8_blockscale", "dg_quant_a8_blockscale",
                  "dg_table_load", "dg_table_check", "dg_sweep"):
         getattr(L, name).restype = S
     _lib = L
@@ -242,6 +245,33 @@ def dg_gemv_bf16(x, W, y=None, ws=None, choice=None, stream=None):
     _ok(lib().dg_gemv_bf16(_ptr(x), _ptr(W), _ptr(y), M, N, K, _ptr(ws), ws.numel(), _stream(stream),
                            _choice(choice)), "dg_gemv_bf16")
     return y
+
+
+def dg_gemv_a8w8_blockscale(x, Wq, sw, y=None, ws=None, choice=None, stream=None):
+    """y[M,N] bf16 = A8W8 block-scaled product of x[M,K] (bf16, quantised per token and
+    128-block inside the call) and Wq[N,K] (e4m3 codes) with block scales sw."""
+    M, K = x.shape
+    N = Wq.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if ws is None:
+        ws = workspace(DG_OP_GEMV_A8W8, M, N, K, device=x.device)
+    _check_dev(x, Wq, sw, y, ws)
+    _ok(lib().dg_gemv_a8w8_blockscale(_ptr(x), _ptr(Wq), _ptr(sw), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
+                                      _stream(stream), _choice(choice)), "dg_gemv_a8w8_blockscale")
+    return y
+
+
+def dg_quant_a8_blockscale(x, q=None, sx=None, stream=None):
+    """(q [M,K] uint8 e4m3 codes, sx [M, ceil(K/128)] fp32): the A8W8 activation quantisation."""
+    M, K = x.shape
+    if q is None:
+        q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((M, (K + 127) // 128), dtype=torch.float32, device=x.device)
+    _check_dev(x, q, sx)
+    _ok(lib().dg_quant_a8_blockscale(_ptr(x), _ptr(q), _ptr(sx), M, K, _stream(stream)), "dg_quant_a8_blockscale")
+    return q, sx
 
 
 def dg_gate_up_silu(x, W_gu, out=None, ws=None, choice=None, stream=None):

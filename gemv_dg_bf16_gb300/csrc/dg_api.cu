@@ -166,6 +166,9 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
         out->params[3] = M <= 1 ? 64 : (M <= 2 ? 128 : (M <= 4 ? 0 : 64));
         out->params[4] = M <= 1 ? 1 : 2;
         break;
+    case DG_OP_GEMV_A8W8:
+        out->variant = DG_VAR_TC;          // fp8 MMA on the quantised activations
+        break;
     default:
         break;
     }
@@ -550,6 +553,32 @@ static dg_status launch_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, 
         return DG_ERR_CUDA;
     }
     return DG_OK;
+}
+
+dg_status dg_gemv_a8w8_blockscale(const void* x, const void* Wq, const float* sw, void* y, int M, int N, int K,
+                                  void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice)
+{
+    if (M < 1 || M > kA8MaxRows || N < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (K % 16 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {x, Wq, sw, y};
+    dg_status s = check_common(ptrs, 4, ws, ws_bytes, dg_workspace_bytes(DG_OP_GEMV_A8W8, M, N, K, 0));
+    if (s != DG_OK) return s;
+    const DeviceInfo* dev = current_device(&s);
+    if (!dev) return s;
+    dg_choice c;
+    if ((s = resolve_choice(DG_OP_GEMV_A8W8, M, N, K, choice, &c)) != DG_OK) return s;
+    if (c.variant != DG_VAR_TC) return DG_ERR_BAD_VARIANT;
+    return launch_tc_a8(dev, c, x, Wq, sw, y, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+dg_status dg_quant_a8_blockscale(const void* x, void* q, float* sx, int M, int K, dg_stream_t stream)
+{
+    if (!x || !q || !sx || M < 1 || K < 1) return DG_ERR_INVALID_ARG;
+    if (K % 16 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(x) || !aligned16(q) || !aligned16(sx)) return DG_ERR_ALIGNMENT;
+    dg_status s;
+    if (!current_device(&s)) return s;
+    return launch_a8_quant(x, q, sx, M, K, reinterpret_cast<cudaStream_t>(stream));
 }
 
 dg_status dg_moe_w1_silu(const void* x, const int32_t* topk_ids, const void* W1, const float* s1,

@@ -33,6 +33,14 @@ struct DeviceInfo;
 dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W,
                     void* out, int M, int N, int K, int ld_out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+// A8W8 block-scaled linear on the tcgen05 family (dg_tc_dense.cu): the fixed K-split
+// of a shape and the launcher; the activation quantisation alone (dg_a8.cu).
+constexpr int kA8MaxRows = 64;
+int tc_a8_nsplit(int N, int K);
+dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x, const void* Wq, const float* sw,
+                       void* y, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t stream);
+dg_status launch_a8_quant(const void* x, void* q, float* sx, int M, int K, cudaStream_t stream);
+
 // tcgen05 fp8 head (dg_tc_head.cu): shared memory for (K, stages) and the launcher.
 size_t tc_head_smem(int K, int stages);
 dg_status launch_tc_head(const DeviceInfo* dev, const dg_choice& c, const void* x, const void* Wq,

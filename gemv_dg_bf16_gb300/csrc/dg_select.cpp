@@ -163,6 +163,7 @@ const char* op_name(int op)
     case DG_OP_HEAD_FP8_ARGMAX: return "head_fp8_argmax";
     case DG_OP_MOE_W1: return "moe_w1_silu";
     case DG_OP_MOE_W2: return "moe_w2";
+    case DG_OP_GEMV_A8W8: return "gemv_a8w8";
     default: return nullptr;
     }
 }
@@ -185,6 +186,7 @@ bool valid_bucket(int m)
 // Returns "" when the choice is acceptable for the op, else the reason.
 std::string check_choice(int op, const dg_choice& c)
 {
+    if (op == DG_OP_GEMV_A8W8 && c.variant != DG_VAR_TC) return "the A8W8 linear runs on the tensor cores only";
     if (c.variant == DG_VAR_TC) {
         if (c.params[0] != 0 && (c.params[0] < 2 || c.params[0] > 8)) return "pipeline stages must be 2..8";
         const bool dense = op == DG_OP_GEMV_BF16 || op == DG_OP_GATE_UP_SILU;
@@ -409,7 +411,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 8; }
+int dg_selection_space(void) { return 9; }
 
 const char* dg_build_id(void) { return build_id(); }
 

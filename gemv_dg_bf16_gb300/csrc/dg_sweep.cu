@@ -159,6 +159,9 @@ struct Problem {
         case DG_OP_MOE_W2:
             return dg_moe_w2(x.p, static_cast<const int32_t*>(rids[rep % nrout].p), static_cast<const float*>(gw.p),
                              w, static_cast<const float*>(s.p), out.p, M, topk, E, K, N, ws.p, ws_bytes, s_, &c);
+        case DG_OP_GEMV_A8W8:
+            return dg_gemv_a8w8_blockscale(x.p, w, static_cast<const float*>(s.p), out.p, M, N, K, ws.p, ws_bytes,
+                                           s_, &c);
         default:
             return DG_ERR_INVALID_ARG;
         }
@@ -188,6 +191,7 @@ dg_status setup(Problem& P, const DeviceInfo* dev)
         wbytes = size_t(P.E) * 2 * N * K; xbytes = size_t(M) * K * 2; P.out_bytes = size_t(M) * P.topk * N * 2; break;
     case DG_OP_MOE_W2:
         wbytes = size_t(P.E) * N * K; xbytes = size_t(M) * P.topk * K * 2; P.out_bytes = size_t(M) * N * 2; break;
+    case DG_OP_GEMV_A8W8: wbytes = size_t(N) * K; xbytes = size_t(M) * K * 2; P.out_bytes = size_t(M) * N * 2; break;
     default: return DG_ERR_INVALID_ARG;
     }
     const bool moe = P.op == DG_OP_MOE_W1 || P.op == DG_OP_MOE_W2;
@@ -207,6 +211,11 @@ dg_status setup(Problem& P, const DeviceInfo* dev)
     P.ws_bytes = dg_workspace_bytes(static_cast<dg_op>(P.op), M, N, K, P.topk);
     if (!P.ws.alloc(P.ws_bytes)) return DG_ERR_CUDA;
     if (cudaMemset(P.ws.p, 0, P.ws_bytes) != cudaSuccess) return DG_ERR_CUDA;
+    if (P.op == DG_OP_GEMV_A8W8) {
+        const size_t nsc = size_t((N + 127) / 128) * ((K + 127) / 128);
+        if (!P.s.alloc(nsc * 4)) return DG_ERR_CUDA;
+        fill_f32<<<64, 256>>>(static_cast<float*>(P.s.p), nsc, 31, 1e-4f, 3e-4f);
+    }
     if (P.op == DG_OP_HEAD_FP8_ARGMAX) {
         if (!P.scale.alloc(4)) return DG_ERR_CUDA;
         fill_f32<<<1, 32>>>(static_cast<float*>(P.scale.p), 1, 19, 1e-3f, 2e-3f);

@@ -32,6 +32,7 @@
 #include <cstdio>
 #include <mutex>
 
+#include "dg_a8.cuh"
 #include "dg_internal.h"
 #include "dg_tc_common.cuh"
 
@@ -57,7 +58,27 @@ struct TcArgs {
     uint16_t* out;
     int ld_out;
     uint8_t* ws;          // status word only (the K-split fold stays on chip)
+    // A8W8 (EPI 2): bf16 activations quantised in the prologue, the weight scales
+    // [ceil(N/128)][kbs], and the most K-blocks one rank holds.
+    const uint16_t* x;
+    const float* sw;
+    int kbs;
+    int xq_blocks;
 };
+
+constexpr int kA8Bufs = 4;                        // A8W8: per-block accumulators in flight
+// A8W8: accumulator full/empty + activations ready, plus one unused slot: the barrier
+// block must stay a multiple of 16 bytes, since the push fold's receive buffer (16-byte
+// st.async / float4 accesses) follows it.
+constexpr int kA8Bars = 2 * kA8Bufs + 2;
+static_assert(kA8Bars % 2 == 0, "keep the barrier block 16-byte aligned");
+
+// A8W8: bytes after the ring for the quantised activations [block][MP rows x 128 B] and
+// the combined scales sx * sw [block][MP].
+__host__ __device__ inline size_t a8_extra_bytes(int xq_blocks, int mp)
+{
+    return static_cast<size_t>(xq_blocks) * mp * (kA8Block + 4);
+}
 
 // Every thread of every CTA of the cluster executes this, unconditionally.
 __device__ __forceinline__ void cluster_sync_all()
@@ -105,7 +126,7 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr)
 template <int EPI>
 __device__ __forceinline__ void emit4(const TcArgs& a, int t, int n, float4 v)
 {
-    if constexpr (EPI == 0) {
+    if constexpr (EPI != 1) {
         uint16_t* dst = a.out + static_cast<size_t>(t) * a.ld_out + n;
         if (n + 3 < a.N && (a.ld_out % 4) == 0) {
             const uint32_t lo = f32_to_bf16_bits(v.x) | (static_cast<uint32_t>(f32_to_bf16_bits(v.y)) << 16);
@@ -149,7 +170,7 @@ __device__ __forceinline__ void store_staged(const TcArgs& a, const float* S, in
     }
     const int q = (r1 - r0) / 8;                      // 8-row pieces per token
     const int n0 = tile * kTileRows + r0;
-    const bool vec = EPI == 0 ? (a.ld_out % 8) == 0 : (a.ld_out % 4) == 0;
+    const bool vec = EPI != 1 ? (a.ld_out % 8) == 0 : (a.ld_out % 4) == 0;
 #pragma unroll 1
     for (int i = etid; i < a.M * q; i += 128) {
         const int t = i / q, c = i - t * q;
@@ -157,7 +178,7 @@ __device__ __forceinline__ void store_staged(const TcArgs& a, const float* S, in
         const float4 lo = *reinterpret_cast<const float4*>(src);
         const float4 hi = *reinterpret_cast<const float4*>(src + 4);
         const int n = n0 + c * 8;
-        if constexpr (EPI == 0) {
+        if constexpr (EPI != 1) {
             if (vec && n + 7 < a.N) {
                 uint4 w;
                 w.x = f32_to_bf16_bits(lo.x) | (static_cast<uint32_t>(f32_to_bf16_bits(lo.y)) << 16);
@@ -166,8 +187,8 @@ __device__ __forceinline__ void store_staged(const TcArgs& a, const float* S, in
                 w.w = f32_to_bf16_bits(hi.z) | (static_cast<uint32_t>(f32_to_bf16_bits(hi.w)) << 16);
                 *reinterpret_cast<uint4*>(a.out + static_cast<size_t>(t) * a.ld_out + n) = w;
             } else {
-                emit4<0>(a, t, n, lo);
-                emit4<0>(a, t, n + 4, hi);
+                emit4<EPI>(a, t, n, lo);
+                emit4<EPI>(a, t, n + 4, hi);
             }
         } else {
             if (vec && n + 7 < a.N) {
@@ -189,19 +210,29 @@ template <int MP, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_dense_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a)
 {
-    constexpr int kXBox = MP * kKB * 2;
+    // EPI 2 (A8W8): e4m3 weights, 128 per stage row; the activations are quantised
+    // into shared memory by the epilogue warps, so a stage holds the weight box only.
+    constexpr bool A8 = EPI == 2;
+    constexpr int KBE = A8 ? kA8Block : kKB;      // K elements per stage
+    constexpr int kXBox = A8 ? 0 : MP * kKB * 2;
     constexpr int kStage = kWBox + kXBox;
-    constexpr uint32_t kCols = MP < 32 ? 32 : MP;
-    constexpr uint32_t kIdesc = tc::idesc_bf16(MP);
+    constexpr uint32_t kCols = A8 ? static_cast<uint32_t>(kA8Bufs * MP) : (MP < 32 ? 32 : MP);
+    constexpr uint32_t kIdesc = A8 ? tc::idesc_f8(MP) : tc::idesc_bf16(MP);
+    constexpr int kExtraBars = A8 ? kA8Bars : 0;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = a.stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kStage);   // full[S], empty[S], accum, recv
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 2);
+    uint8_t* xq = smem + S * kStage;                                            // A8: [block][MP x 128 B]
+    float* sxs = reinterpret_cast<float*>(xq + static_cast<size_t>(a.xq_blocks) * MP * kA8Block);   // A8: [block][MP]
+    const size_t xtra = A8 ? a8_extra_bytes(a.xq_blocks, MP) : 0;
+    // full[S], empty[S], accum, recv (+ A8: acc_full[4], acc_empty[4], x_ready)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * kStage + xtra);
+    const int nbars = 2 * S + 2 + kExtraBars;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + nbars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     // Push fold: rows pushed here by every rank, [rank][slice row][mq] fp32.
-    float* recv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + (2 * S + 2) * 8 + 16);
+    float* recv = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + nbars * 8 + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool clustered = a.nsplit > 1;
@@ -213,6 +244,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2 * S + 2; ++s) tc::bar_init(tc::su32(bars + s), 1);
+        if constexpr (A8) {
+            for (int b = 0; b < kA8Bufs; ++b) {
+                tc::bar_init(tc::su32(bars + 2 * S + 2 + b), 1);             // MMA commit
+                tc::bar_init(tc::su32(bars + 2 * S + 2 + kA8Bufs + b), 4);   // one per epilogue warp
+            }
+            tc::bar_init(tc::su32(bars + 2 * S + 2 + 2 * kA8Bufs), 1);
+        }
         if (clustered && a.push) {
             // every rank pushes this rank's slice of rows, mq tokens each
             const int rows = slice_lo(split + 1, a.nsplit) - slice_lo(split, a.nsplit);
@@ -234,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const uint32_t full0 = tc::su32(bars), empty0 = tc::su32(bars + S), accum = tc::su32(bars + 2 * S);
     const uint32_t recv_bar = tc::su32(bars + 2 * S + 1);
+    const uint32_t accf0 = tc::su32(bars + 2 * S + 2), acce0 = accf0 + 8 * kA8Bufs, xready = accf0 + 16 * kA8Bufs;
 
     pdl_launch_dependents();
     if (warp == 0) {
@@ -246,20 +285,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < pre; ++i) {
                 const uint32_t dst = tc::su32(smem + i * kStage);
                 tc::bar_expect_tx(full0 + 8 * i, kStage);
-                tc::tma_2d_hint(dst, &tmW, (kb0 + i) * kKB, tile * kTileRows, full0 + 8 * i, once);
+                tc::tma_2d_hint(dst, &tmW, (kb0 + i) * KBE, tile * kTileRows, full0 + 8 * i, once);
             }
             pdl_wait();
-            for (int i = 0; i < pre; ++i)
-                tc::tma_2d(tc::su32(smem + i * kStage) + kWBox, &tmX, (kb0 + i) * kKB, 0, full0 + 8 * i);
+            if constexpr (!A8)
+                for (int i = 0; i < pre; ++i)
+                    tc::tma_2d(tc::su32(smem + i * kStage) + kWBox, &tmX, (kb0 + i) * kKB, 0, full0 + 8 * i);
             for (int i = pre; i < nkb; ++i) {
                 const int s = i % S;
                 const uint32_t round = static_cast<uint32_t>(i / S);
                 if (!tc::bar_wait(empty0 + 8 * s, (round & 1u) ^ 1u, abort_flag)) break;
                 const uint32_t dst = tc::su32(smem + s * kStage);
                 tc::bar_expect_tx(full0 + 8 * s, kStage);
-                const int k = (kb0 + i) * kKB;
+                const int k = (kb0 + i) * KBE;
                 tc::tma_2d_hint(dst, &tmW, k, tile * kTileRows, full0 + 8 * s, once);
-                tc::tma_2d(dst + kWBox, &tmX, k, 0, full0 + 8 * s);
+                if constexpr (!A8) tc::tma_2d(dst + kWBox, &tmX, k, 0, full0 + 8 * s);
             }
         } else {
             pdl_wait();
@@ -267,17 +307,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         pdl_wait();
         if (lane == 0) {
-            for (int i = 0; i < nkb; ++i) {
+            // A8: the quantised activations must be in place first
+            const bool xok = !A8 || tc::bar_wait(xready, 0, abort_flag);
+            for (int i = 0; xok && i < nkb; ++i) {
                 const int s = i % S;
                 const uint32_t round = static_cast<uint32_t>(i / S);
                 if (!tc::bar_wait(full0 + 8 * s, round & 1u, abort_flag)) break;
-                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t wa = tc::su32(smem + s * kStage), xa = wa + kWBox;
+                const uint32_t wa = tc::su32(smem + s * kStage);
+                if constexpr (A8) {
+                    // One K-block (128 elements, 4 x K=32) into accumulator b, from zero;
+                    // the epilogue scales and folds it, then frees the accumulator.
+                    const int b = i % kA8Bufs;
+                    if (i >= kA8Bufs &&
+                        !tc::bar_wait(acce0 + 8 * b, static_cast<uint32_t>(i / kA8Bufs - 1) & 1u, abort_flag))
+                        break;
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t xa = tc::su32(xq + static_cast<size_t>(i) * MP * kA8Block);
 #pragma unroll
-                for (int kk = 0; kk < kKB / 16; ++kk)
-                    tc::mma_bf16(tmem, tc::sw128_desc(wa + kk * 32), tc::sw128_desc(xa + kk * 32), kIdesc,
-                             (i > 0 || kk > 0) ? 1u : 0u);
-                tc::commit(empty0 + 8 * s);
+                    for (int kk = 0; kk < kA8Block / 32; ++kk)
+                        tc::mma_f8(tmem + static_cast<uint32_t>(b * MP), tc::sw128_desc(wa + kk * 32),
+                                   tc::sw128_desc(xa + kk * 32), kIdesc, kk > 0 ? 1u : 0u);
+                    tc::commit(empty0 + 8 * s);
+                    tc::commit(accf0 + 8 * b);
+                } else {
+                    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                    const uint32_t xa = wa + kWBox;
+#pragma unroll
+                    for (int kk = 0; kk < kKB / 16; ++kk)
+                        tc::mma_bf16(tmem, tc::sw128_desc(wa + kk * 32), tc::sw128_desc(xa + kk * 32), kIdesc,
+                                     (i > 0 || kk > 0) ? 1u : 0u);
+                    tc::commit(empty0 + 8 * s);
+                }
             }
             tc::commit(accum);           // fires once every MMA issued above has completed
         }
@@ -286,6 +346,107 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Epilogue warps 2..5 -> TMEM lane quarter (warp % 4).
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        if constexpr (A8) {
+            const int et = threadIdx.x - 64;
+            // (1) Quantise this rank's K-blocks of the M token rows, 16 elements per
+            // thread and 8 threads per (block, token); eight tasks' loads are issued
+            // before any is used.  Rows M..MP-1 get zero codes and scales (their
+            // columns are never stored).  sxs holds the block's combined scale sx * sw.
+            constexpr int kU = 8;
+            const int tasks = nkb * a.M * 8;
+#pragma unroll 1
+            for (int base = 0; base < tasks; base += 128 * kU) {
+                uint4 raw[kU][2];
+                float swv[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int qi = base + u * 128 + et;
+                    const int g = qi >> 3, t = g % a.M, i = g / a.M;
+                    const int k0 = (kb0 + i) * kA8Block + (qi & 7) * 16;
+                    raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+                    swv[u] = 0.0f;
+                    if (qi < tasks) {
+                        if (k0 < a.K) {
+                            const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.K + k0);
+                            raw[u][0] = src[0];
+                            raw[u][1] = src[1];
+                        }
+                        swv[u] = a.sw[static_cast<size_t>(tile) * a.kbs + kb0 + i];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int qi = base + u * 128 + et;
+                    const int g = qi >> 3, t = g % a.M, i = g / a.M, ch = qi & 7;
+                    float v[16];
+                    a8_unpack16(raw[u][0], raw[u][1], v);
+                    const float amax = a8_block_amax(v);          // every lane takes part
+                    if (qi < tasks) {
+                        *reinterpret_cast<uint4*>(xq + static_cast<size_t>(i) * MP * kA8Block + tc::sw128_offset(t, ch)) =
+                            a8_codes(v, a8_recip_scale(amax));
+                        if (ch == 0) sxs[i * MP + t] = __fmul_rn(a8_scale(amax), swv[u]);
+                    }
+                }
+            }
+            if (a.M < MP) {
+                const int dead = MP - a.M;
+                for (int z = et; z < nkb * dead * 8; z += 128) {
+                    const int i = z / (dead * 8), r = z - i * dead * 8, t = a.M + (r >> 3), ch = r & 7;
+                    *reinterpret_cast<uint4*>(xq + static_cast<size_t>(i) * MP * kA8Block + tc::sw128_offset(t, ch)) =
+                        make_uint4(0, 0, 0, 0);
+                    if (ch == 0) sxs[i * MP + t] = 0.0f;
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            asm volatile("bar.sync 1, 128;" ::: "memory");
+            if (et == 0) tc::bar_arrive(xready);
+            // (2) Fold the blocks in ascending order: tot = fma(p_b, sx_b * sw_b, tot), from 0.
+            float tot[MP];
+#pragma unroll
+            for (int j = 0; j < MP; ++j) tot[j] = 0.0f;
+            bool all_in = true;
+#pragma unroll 1
+            for (int i = 0; i < nkb; ++i) {
+                const int b = i % kA8Bufs;
+                const bool w = tc::bar_wait(accf0 + 8 * b, static_cast<uint32_t>(i / kA8Bufs) & 1u, abort_flag);
+                if (!__all_sync(kFull, w)) {
+                    all_in = false;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+                for (int c = 0; c < MP / 16; ++c) {
+                    if (c * 16 >= a.M) break;
+                    uint32_t v[16];
+                    tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * MP + c * 16), v);
+                    const float4* sc4 = reinterpret_cast<const float4*>(sxs + i * MP + c * 16);
+#pragma unroll
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const float4 sc = sc4[j4];
+                        const int j = c * 16 + 4 * j4;
+                        tot[j + 0] = __fmaf_rn(__uint_as_float(v[4 * j4 + 0]), sc.x, tot[j + 0]);
+                        tot[j + 1] = __fmaf_rn(__uint_as_float(v[4 * j4 + 1]), sc.y, tot[j + 1]);
+                        tot[j + 2] = __fmaf_rn(__uint_as_float(v[4 * j4 + 2]), sc.z, tot[j + 2]);
+                        tot[j + 3] = __fmaf_rn(__uint_as_float(v[4 * j4 + 3]), sc.w, tot[j + 3]);
+                    }
+                }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) tc::bar_arrive(acce0 + 8 * b);
+            }
+            // (3) The rank's totals into TMEM columns 0..MP-1, where the tail below reads a
+            // finished accumulator (every MMA has completed by now).
+            if (all_in) {
+#pragma unroll
+                for (int c = 0; c < MP / 16; ++c) {
+                    uint32_t v[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(tot[c * 16 + j]);
+                    tc::tmem_st16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(c * 16), v);
+                }
+                tc::tmem_st_wait();
+            }
+        }
         const bool ok = tc::bar_wait(accum, 0, abort_flag);
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         // `good` may differ between threads when a wait ran out; every named barrier
@@ -439,8 +600,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
+// 2-D tiled map, 128-byte swizzle: bf16 elements, or bytes (e4m3 codes) when `u8`.
 bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint32_t box_inner,
-               uint32_t box_outer)
+               uint32_t box_outer, bool u8 = false)
 {
     std::call_once(g_encode_once, [] {
         void* fn = nullptr;
@@ -453,10 +615,10 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, 
     });
     if (!g_encode) return false;
     const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint64_t strides[1] = {inner * (u8 ? 1 : 2)};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+    return g_encode(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -469,17 +631,20 @@ const void* tc_fn()
 
 const void* tc_lookup(int mp, int epi)
 {
-    switch (mp * 2 + epi) {
-    case 16 * 2 + 0: return tc_fn<16, 0>();
-    case 16 * 2 + 1: return tc_fn<16, 1>();
-    case 32 * 2 + 0: return tc_fn<32, 0>();
-    case 32 * 2 + 1: return tc_fn<32, 1>();
-    case 64 * 2 + 0: return tc_fn<64, 0>();
-    case 64 * 2 + 1: return tc_fn<64, 1>();
-    case 128 * 2 + 0: return tc_fn<128, 0>();
-    case 128 * 2 + 1: return tc_fn<128, 1>();
-    case 256 * 2 + 0: return tc_fn<256, 0>();
-    case 256 * 2 + 1: return tc_fn<256, 1>();
+    switch (mp * 4 + epi) {
+    case 16 * 4 + 0: return tc_fn<16, 0>();
+    case 16 * 4 + 1: return tc_fn<16, 1>();
+    case 16 * 4 + 2: return tc_fn<16, 2>();
+    case 32 * 4 + 0: return tc_fn<32, 0>();
+    case 32 * 4 + 1: return tc_fn<32, 1>();
+    case 32 * 4 + 2: return tc_fn<32, 2>();
+    case 64 * 4 + 0: return tc_fn<64, 0>();
+    case 64 * 4 + 1: return tc_fn<64, 1>();
+    case 64 * 4 + 2: return tc_fn<64, 2>();
+    case 128 * 4 + 0: return tc_fn<128, 0>();
+    case 128 * 4 + 1: return tc_fn<128, 1>();
+    case 256 * 4 + 0: return tc_fn<256, 0>();
+    case 256 * 4 + 1: return tc_fn<256, 1>();
     default: return nullptr;
     }
 }
@@ -592,6 +757,121 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
         return DG_ERR_CUDA;
     if (occupancy(fn, kThreads, smem) < 1) return DG_ERR_UNSUPPORTED_SHAPE;
     void* args[] = {&tmW, &tmX, &a};
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.tiles * a.nsplit));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(a.nsplit);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+        cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    return DG_OK;
+}
+
+}  // namespace dg
+
+namespace dg {
+
+// ------------------------------------------------------------------ A8W8 blockscale
+
+int tc_a8_nsplit(int N, int K)
+{
+    const int tiles = (N + kTileRows - 1) / kTileRows;
+    const int nkb = (K + kA8Block - 1) / kA8Block;
+    // About 160 CTAs (two per SM), and at most 8 K-blocks of quantised activations per
+    // rank (64 KB at 64 tokens); a function of the shape alone, so a row's bits do not
+    // depend on how many rows share the call.
+    int ns = (160 + tiles - 1) / tiles;
+    const int by_smem = (nkb + 7) / 8;
+    if (ns < by_smem) ns = by_smem;
+    if (ns > kMaxCluster) ns = kMaxCluster;
+    if (ns > nkb) ns = nkb;
+    if (ns < 1) ns = 1;
+    return ns;
+}
+
+namespace {
+
+size_t smem_bytes_a8(int mp, int stages, size_t recv, int xq_blocks)
+{
+    return 1024 + static_cast<size_t>(stages) * kWBox + a8_extra_bytes(xq_blocks, mp) +
+           (2 * stages + 2 + kA8Bars) * 8 + 16 + recv;
+}
+
+}  // namespace
+
+dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x, const void* Wq, const float* sw,
+                       void* y, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    (void)dev;
+    if (M < 1 || M > kA8MaxRows || K % 16 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
+    for (int i = 1; i < 6; ++i)
+        if (c.params[i] != 0) return DG_ERR_BAD_VARIANT;
+    const int mp = tc_mp(M);
+    const void* fn = tc_lookup(mp, 2);
+    if (!fn) return DG_ERR_BAD_VARIANT;
+    const int ns = tc_a8_nsplit(N, K);
+    const int nkb = (K + kA8Block - 1) / kA8Block;
+    const int xq_blocks = (nkb + ns - 1) / ns;
+    const int mq = (M + 3) & ~3;
+    size_t recv = mq <= kPushMaxTokens ? recv_bytes(ns, mq) : 0;
+    // Two CTAs per SM when at least two stages fit beside the activations, else one
+    // CTA per SM with a deeper ring.
+    int stages = c.params[0];
+    if (stages == 0) {
+        stages = 5;
+        while (stages > 2 && smem_bytes_a8(mp, stages, recv, xq_blocks) > kCoResidentSmem) --stages;
+        if (smem_bytes_a8(mp, stages, recv, xq_blocks) > kCoResidentSmem) {
+            stages = 8;
+            while (stages > 2 && smem_bytes_a8(mp, stages, recv, xq_blocks) > kMaxDynSmem) --stages;
+        }
+    }
+    if (stages < 2 || stages > 8) return DG_ERR_BAD_VARIANT;
+    // The epilogue stages the tile (or parks the K-split partial) in the ring.
+    const size_t part_bytes = static_cast<size_t>(mp) * kTileRows * 4;
+    if (static_cast<size_t>(stages) * kWBox < part_bytes) return DG_ERR_BAD_VARIANT;
+    if (recv > 0 && smem_bytes_a8(mp, stages, recv, xq_blocks) > kMaxDynSmem) recv = 0;
+    size_t smem = smem_bytes_a8(mp, stages, recv, xq_blocks);
+    if (smem > kMaxDynSmem) return DG_ERR_UNSUPPORTED_SHAPE;
+    // Never more co-resident CTAs than their TMEM columns (4 x MP each) fit in the SM's
+    // 512: a CTA waiting in tcgen05.alloc while its cluster peers wait for it would hang.
+    const size_t per_sm = 228 * 1024;
+    const size_t min_smem = per_sm / (512 / (kA8Bufs * mp) + 1) + 1024;
+    if (smem < min_smem) smem = min_smem;
+    if (ws_bytes < kWsData) return DG_ERR_WORKSPACE_TOO_SMALL;
+    TcArgs a{};
+    a.N = N;
+    a.K = K;
+    a.M = M;
+    a.tiles = (N + kTileRows - 1) / kTileRows;
+    a.nkb = nkb;
+    a.nsplit = ns;
+    a.push = recv > 0 ? 1 : 0;
+    a.mq = mq;
+    a.slice_max = slice_max(ns);
+    a.stages = stages;
+    a.out = static_cast<uint16_t*>(y);
+    a.ld_out = N;
+    a.ws = static_cast<uint8_t*>(ws);
+    a.x = static_cast<const uint16_t*>(x);
+    a.sw = sw;
+    a.kbs = nkb;
+    a.xq_blocks = xq_blocks;
+    CUtensorMap tmW;
+    if (!encode_2d(&tmW, Wq, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kA8Block, kTileRows, true))
+        return DG_ERR_CUDA;
+    if (occupancy(fn, kThreads, smem) < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+    void* args[] = {&tmW, &tmW, &a};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.tiles * a.nsplit));
     cfg.blockDim = dim3(kThreads);

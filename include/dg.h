@@ -71,7 +71,8 @@ typedef enum {
     DG_OP_HEAD_FP8_ARGMAX = 2,
     DG_OP_MOE_W1 = 3,
     DG_OP_MOE_W2 = 4,
-    DG_OP_COUNT = 5
+    DG_OP_GEMV_A8W8 = 5,
+    DG_OP_COUNT = 6
 } dg_op;
 
 /* Kernel families.  One family serves one (op, M) bucket; variants inside a
@@ -271,6 +272,29 @@ dg_status dg_moe_w1_silu(const void* x, const int32_t* topk_ids, const void* W1,
 dg_status dg_moe_w2(const void* a, const int32_t* topk_ids, const float* gw, const void* W2,
                     const float* s2, void* y, int M, int topk, int E, int I, int Nout, void* ws,
                     size_t ws_bytes, dg_stream_t stream, const dg_choice* choice);
+
+/* A8W8 block-scaled linear with the activation quantisation fused in as its prologue
+ * ("Decode optimization round 3", "Retained change 2: decode-M rows for the A8W8
+ * bpreshuffle table" -- the A8W8 blockscale GEMM at decode rows -- and "Rejected
+ * paths" / "Remaining headroom" -- quantisation kernels fused into the GEMM).
+ * Blocks are 128 wide along K.  Per token m and K-block b, in binary32:
+ *   amax    = max(max_{k in b} |x[m, k]|, 2^-32)
+ *   q[m, k] = e4m3(x[m, k] * (448 / amax))     round to nearest even, saturating
+ *   sx[m,b] = amax / 448
+ *   y[m, n] = bf16_rn( sum_b  P_b * (sx[m, b] * sw[n / 128, b]) ),
+ *             P_b = sum_{k in b} e4m3(q[m, k]) * e4m3(Wq[n, k])      fp32
+ * x [M, K] bf16, Wq [N, K] e4m3 codes, sw [ceil(N/128), ceil(K/128)] fp32 (one scale
+ * per 128 x 128 weight block, row-major), y [M, N] bf16.  1 <= M <= 64, K % 16 == 0.
+ * Runs on the tensor cores only (DG_VAR_TC; params[0] pipeline stages); the K-split
+ * is fixed by (N, K), so output row m depends on input row m alone at every M.
+ * Non-finite activations give NaN outputs for their token.  ws: status word only. */
+dg_status dg_gemv_a8w8_blockscale(const void* x, const void* Wq, const float* sw, void* y, int M, int N, int K,
+                                  void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice);
+
+/* The quantisation step of dg_gemv_a8w8_blockscale on its own (the same device code):
+ * q [M, K] e4m3 codes and sx [M, ceil(K/128)] fp32, as defined there.  M >= 1,
+ * K % 16 == 0; asynchronous on `stream`; argument errors return before any launch. */
+dg_status dg_quant_a8_blockscale(const void* x, void* q, float* sx, int M, int K, dg_stream_t stream);
 
 /* ---------------------------------------------------------------- selection */
 

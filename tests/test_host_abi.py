@@ -243,3 +243,30 @@ def test_tc_split_rule_parameter_checked(tmp_path):
     assert s == 6 and "K-split rule" in why
     s, _, why = _check(_table(tmp_path, entries=ent("moe_w1_silu", [0, 1])))
     assert s == 6 and "unused tensor-core parameter" in why
+
+
+def test_a8w8_select_and_argument_errors():
+    for M in (1, 2, 5, 16, 33, 64):
+        c = dg.dg_select(dg.DG_OP_GEMV_A8W8, M, 8192, 4096)
+        assert c.variant == dg.DG_VAR_TC and c.from_table == 0
+    assert dg.dg_workspace_bytes(dg.DG_OP_GEMV_A8W8, 64, 8192, 4096) >= 16
+    L = dg.lib()
+    P = ctypes.c_void_p
+    call = lambda x=A, W=A, s=A, y=A, M=2, N=64, K=256, ws=A, wsb=1 << 16, c=None: L.dg_gemv_a8w8_blockscale(
+        P(x), P(W), P(s), P(y), M, N, K, P(ws), wsb, None, c)
+    assert call(M=0) == 1 and call(M=65) == 1 and call(N=0) == 1
+    assert call(K=264) == 3                       # K % 16
+    assert call(s=0) == 1 and call(s=U) == 2 and call(W=U) == 2
+    assert call(wsb=8) == 4
+    bad = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0)
+    assert dg.lib().dg_quant_a8_blockscale(P(A), P(A), P(A), 2, 40, None) == 3
+    assert dg.lib().dg_quant_a8_blockscale(P(A), P(U), P(A), 2, 64, None) == 2
+    assert dg.lib().dg_quant_a8_blockscale(None, P(A), P(A), 2, 64, None) == 1
+
+
+def test_a8w8_table_refuses_cuda_core_pick(tmp_path):
+    ent = [{"op": "gemv_a8w8", "M": 4, "N": 64, "K": 64, "pick": {"variant": 1, "params": [4, 8]}}]
+    s, _, why = _check(_table(tmp_path, entries=ent))
+    assert s == 6 and "tensor cores only" in why
+    ent = [{"op": "gemv_a8w8", "M": 4, "N": 64, "K": 64, "pick": {"variant": 3, "params": [4]}}]
+    assert _check(_table(tmp_path, entries=ent))[0] == 0
