@@ -67,10 +67,12 @@ struct TcArgs {
 };
 
 constexpr int kA8Bufs = 4;                        // A8W8: per-block accumulators in flight
-// A8W8: accumulator full/empty + activations ready, plus one unused slot: the barrier
-// block must stay a multiple of 16 bytes, since the push fold's receive buffer (16-byte
-// st.async / float4 accesses) follows it.
-constexpr int kA8Bars = 2 * kA8Bufs + 2;
+// A8W8: accumulator full/empty, and one "activations quantised" barrier per K-block a
+// rank holds (at most kA8MaxBlocks).  The count stays even: the barrier block must stay a
+// multiple of 16 bytes, since the push fold's receive buffer (16-byte st.async / float4
+// accesses) follows it.
+constexpr int kA8MaxBlocks = 16;
+constexpr int kA8Bars = 2 * kA8Bufs + kA8MaxBlocks;
 static_assert(kA8Bars % 2 == 0, "keep the barrier block 16-byte aligned");
 
 // A8W8: bytes after the ring for the quantised activations [block][MP rows x 128 B] and
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::bar_init(tc::su32(bars + 2 * S + 2 + b), 1);             // MMA commit
                 tc::bar_init(tc::su32(bars + 2 * S + 2 + kA8Bufs + b), 4);   // one per epilogue warp
             }
-            tc::bar_init(tc::su32(bars + 2 * S + 2 + 2 * kA8Bufs), 1);
+            for (int i = 0; i < kA8MaxBlocks; ++i) tc::bar_init(tc::su32(bars + 2 * S + 2 + 2 * kA8Bufs + i), 1);
         }
         if (clustered && a.push) {
             // every rank pushes this rank's slice of rows, mq tokens each
@@ -272,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_holder;
     const uint32_t full0 = tc::su32(bars), empty0 = tc::su32(bars + S), accum = tc::su32(bars + 2 * S);
     const uint32_t recv_bar = tc::su32(bars + 2 * S + 1);
-    const uint32_t accf0 = tc::su32(bars + 2 * S + 2), acce0 = accf0 + 8 * kA8Bufs, xready = accf0 + 16 * kA8Bufs;
+    const uint32_t accf0 = tc::su32(bars + 2 * S + 2), acce0 = accf0 + 8 * kA8Bufs, xfull0 = accf0 + 16 * kA8Bufs;
 
     pdl_launch_dependents();
     if (warp == 0) {
@@ -307,9 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         pdl_wait();
         if (lane == 0) {
-            // A8: the quantised activations must be in place first
-            const bool xok = !A8 || tc::bar_wait(xready, 0, abort_flag);
-            for (int i = 0; xok && i < nkb; ++i) {
+            for (int i = 0; i < nkb; ++i) {
                 const int s = i % S;
                 const uint32_t round = static_cast<uint32_t>(i / S);
                 if (!tc::bar_wait(full0 + 8 * s, round & 1u, abort_flag)) break;
@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // One K-block (128 elements, 4 x K=32) into accumulator b, from zero;
                     // the epilogue scales and folds it, then frees the accumulator.
                     const int b = i % kA8Bufs;
+                    if (!tc::bar_wait(xfull0 + 8 * i, 0, abort_flag)) break;        // block i quantised
                     if (i >= kA8Bufs &&
                         !tc::bar_wait(acce0 + 8 * b, static_cast<uint32_t>(i / kA8Bufs - 1) & 1u, abort_flag))
                         break;
@@ -348,58 +349,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         if constexpr (A8) {
             const int et = threadIdx.x - 64;
-            // (1) Quantise this rank's K-blocks of the M token rows, 16 elements per
-            // thread and 8 threads per (block, token); eight tasks' loads are issued
-            // before any is used.  Rows M..MP-1 get zero codes and scales (their
-            // columns are never stored).  sxs holds the block's combined scale sx * sw.
-            constexpr int kU = 8;
-            const int tasks = nkb * a.M * 8;
-#pragma unroll 1
-            for (int base = 0; base < tasks; base += 128 * kU) {
-                uint4 raw[kU][2];
-                float swv[kU];
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int qi = base + u * 128 + et;
-                    const int g = qi >> 3, t = g % a.M, i = g / a.M;
-                    const int k0 = (kb0 + i) * kA8Block + (qi & 7) * 16;
-                    raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
-                    swv[u] = 0.0f;
-                    if (qi < tasks) {
-                        if (k0 < a.K) {
-                            const uint4* src = reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * a.K + k0);
-                            raw[u][0] = src[0];
-                            raw[u][1] = src[1];
-                        }
-                        swv[u] = a.sw[static_cast<size_t>(tile) * a.kbs + kb0 + i];
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int qi = base + u * 128 + et;
-                    const int g = qi >> 3, t = g % a.M, i = g / a.M, ch = qi & 7;
-                    float v[16];
-                    a8_unpack16(raw[u][0], raw[u][1], v);
-                    const float amax = a8_block_amax(v);          // every lane takes part
-                    if (qi < tasks) {
-                        *reinterpret_cast<uint4*>(xq + static_cast<size_t>(i) * MP * kA8Block + tc::sw128_offset(t, ch)) =
-                            a8_codes(v, a8_recip_scale(amax));
-                        if (ch == 0) sxs[i * MP + t] = __fmul_rn(a8_scale(amax), swv[u]);
-                    }
-                }
-            }
-            if (a.M < MP) {
-                const int dead = MP - a.M;
-                for (int z = et; z < nkb * dead * 8; z += 128) {
-                    const int i = z / (dead * 8), r = z - i * dead * 8, t = a.M + (r >> 3), ch = r & 7;
+            // (1) Rows M..MP-1 of every block get zero codes and scales (their columns
+            // are never stored); chunk z = (i * MP + t) * 8 + ch.
+            const int live_rows = a.M;
+            if (live_rows < MP) {
+                for (int z = et; z < nkb * MP * 8; z += 128) {
+                    const int ch = z & 7, t = (z >> 3) & (MP - 1), i = z / (MP * 8);
+                    if (t < live_rows) continue;
                     *reinterpret_cast<uint4*>(xq + static_cast<size_t>(i) * MP * kA8Block + tc::sw128_offset(t, ch)) =
                         make_uint4(0, 0, 0, 0);
                     if (ch == 0) sxs[i * MP + t] = 0.0f;
                 }
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (et == 0) tc::bar_arrive(xready);
+            // (2) Quantise the live rows: 8 threads per (block, token) group, 16 elements
+            // each, groups in block-major order g = i * M + t, 16 groups per slot of the
+            // 128 threads.  Eight slots' loads are issued before any is used; after each
+            // slot the blocks it completed are released to the MMA warp (x_full[i]), so
+            // the first MMAs overlap the rest of the quantisation.  sxs holds the block's
+            // combined scale sx * sw.
+            constexpr int kU = 8;
+            const int groups = nkb * live_rows;
+            const int step_i = 16 / live_rows, step_t = 16 % live_rows;
+            int gi = (et >> 3) / live_rows, gt = (et >> 3) % live_rows;     // (i, t) of this thread's next group
+            int released = 0;
+#pragma unroll 1
+            for (int g0 = 0; g0 < groups; g0 += 16 * kU) {
+                uint4 raw[kU][2];
+                float swv[kU];
+                int ii[kU], tt[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int g = g0 + u * 16 + (et >> 3);
+                    ii[u] = gi;
+                    tt[u] = gt;
+                    gi += step_i;
+                    gt += step_t;
+                    if (gt >= live_rows) {
+                        gt -= live_rows;
+                        ++gi;
+                    }
+                    const int k0 = (kb0 + ii[u]) * kA8Block + (et & 7) * 16;
+                    raw[u][0] = raw[u][1] = make_uint4(0, 0, 0, 0);
+                    swv[u] = 0.0f;
+                    if (g < groups) {
+                        if (k0 < a.K) {
+                            const uint4* src =
+                                reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(tt[u]) * a.K + k0);
+                            raw[u][0] = src[0];
+                            raw[u][1] = src[1];
+                        }
+                        swv[u] = a.sw[static_cast<size_t>(tile) * a.kbs + kb0 + ii[u]];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int g = g0 + u * 16 + (et >> 3);
+                    float v[16];
+                    a8_unpack16(raw[u][0], raw[u][1], v);
+                    const float amax = a8_block_amax(v);          // every lane takes part
+                    if (g < groups) {
+                        *reinterpret_cast<uint4*>(xq + static_cast<size_t>(ii[u]) * MP * kA8Block +
+                                                  tc::sw128_offset(tt[u], et & 7)) = a8_codes(v, a8_recip_scale(amax));
+                        if ((et & 7) == 0) sxs[ii[u] * MP + tt[u]] = __fmul_rn(a8_scale(amax), swv[u]);
+                    }
+                    const int gend = g0 + (u + 1) * 16 < groups ? g0 + (u + 1) * 16 : groups;
+                    if ((released + 1) * live_rows <= gend) {     // the same decision in every thread
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        asm volatile("bar.sync 1, 128;" ::: "memory");
+                        while ((released + 1) * live_rows <= gend) {
+                            if (et == 0) tc::bar_arrive(xfull0 + 8 * released);
+                            ++released;
+                        }
+                    }
+                }
+            }
             // (2) Fold the blocks in ascending order: tot = fma(p_b, sx_b * sw_b, tot), from 0.
             float tot[MP];
 #pragma unroll
@@ -823,6 +846,7 @@ dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x,
     const int ns = tc_a8_nsplit(N, K);
     const int nkb = (K + kA8Block - 1) / kA8Block;
     const int xq_blocks = (nkb + ns - 1) / ns;
+    if (xq_blocks > kA8MaxBlocks) return DG_ERR_UNSUPPORTED_SHAPE;
     const int mq = (M + 3) & ~3;
     size_t recv = mq <= kPushMaxTokens ? recv_bytes(ns, mq) : 0;
     // Two CTAs per SM when at least two stages fit beside the activations, else one
