@@ -37,6 +37,7 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
 // of a shape and the launcher; the activation quantisation alone (dg_a8.cu).
 constexpr int kA8MaxRows = 64;
 int tc_a8_nsplit(int N, int K);
+size_t a8_workspace_bytes(int M, int K);
 dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x, const void* Wq, const float* sw,
                        void* y, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t stream);
 dg_status launch_a8_quant(const void* x, void* q, float* sx, int M, int K, cudaStream_t stream);

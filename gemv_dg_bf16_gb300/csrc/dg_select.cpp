@@ -189,8 +189,10 @@ std::string check_choice(int op, const dg_choice& c)
     if (op == DG_OP_GEMV_A8W8 && c.variant != DG_VAR_TC) return "the A8W8 linear runs on the tensor cores only";
     if (c.variant == DG_VAR_TC) {
         if (c.params[0] != 0 && (c.params[0] < 2 || c.params[0] > 8)) return "pipeline stages must be 2..8";
-        const bool dense = op == DG_OP_GEMV_BF16 || op == DG_OP_GATE_UP_SILU;
-        if (dense && c.params[1] != 0 && c.params[1] != 1) return "tensor-core K-split rule must be 0 or 1";
+        const bool dense = op == DG_OP_GEMV_BF16 || op == DG_OP_GATE_UP_SILU || op == DG_OP_GEMV_A8W8;
+        if (dense && c.params[1] != 0 && c.params[1] != 1)
+            return op == DG_OP_GEMV_A8W8 ? "A8W8 quantisation launch flag must be 0 or 1"
+                                         : "tensor-core K-split rule must be 0 or 1";
         for (int i = dense ? 2 : 1; i < 6; ++i)
             if (c.params[i] != 0) return "unused tensor-core parameter set";
         return "";

@@ -110,6 +110,10 @@ std::vector<dg_choice> candidates(int op, const dg_choice& def)
             dg_choice c = mk(DG_VAR_TC, st);
             c.params[1] = def.params[1];       // the K-split rule is part of the arithmetic
             add(c);
+            if (op == DG_OP_GEMV_A8W8) {       // quantisation fused or in a launch of its own
+                c.params[1] = 1 - def.params[1];
+                add(c);
+            }
         }
     } else if (op == DG_OP_MOE_W1 || op == DG_OP_MOE_W2) {
         const bool w1 = op == DG_OP_MOE_W1;

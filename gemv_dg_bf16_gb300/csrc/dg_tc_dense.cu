@@ -64,6 +64,10 @@ struct TcArgs {
     const float* sw;
     int kbs;
     int xq_blocks;
+    // A8W8 with the quantisation done by a preceding launch: the codes come by TMA
+    // (tmX over q [M, K]) and the activation scales from sxg [M, kbs].
+    int preq;
+    const float* sxg;
 };
 
 constexpr int kA8Bufs = 4;                        // A8W8: per-block accumulators in flight
@@ -293,6 +297,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if constexpr (!A8)
                 for (int i = 0; i < pre; ++i)
                     tc::tma_2d(tc::su32(smem + i * kStage) + kWBox, &tmX, (kb0 + i) * kKB, 0, full0 + 8 * i);
+            if constexpr (A8)
+                if (a.preq)
+                    // every block's codes at once (rows M..MP-1 read as zeros), each
+                    // completing its own x_full barrier
+                    for (int i = 0; i < nkb; ++i) {
+                        tc::bar_expect_tx(xfull0 + 8 * i, MP * kA8Block);
+                        tc::tma_2d(tc::su32(xq + static_cast<size_t>(i) * MP * kA8Block), &tmX, (kb0 + i) * kA8Block,
+                                   0, xfull0 + 8 * i);
+                    }
             for (int i = pre; i < nkb; ++i) {
                 const int s = i % S;
                 const uint32_t round = static_cast<uint32_t>(i / S);
@@ -349,10 +362,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;
         if constexpr (A8) {
             const int et = threadIdx.x - 64;
+            if (a.preq) {
+                // The codes arrive by TMA; the combined scales sx * sw of the live rows.
+                for (int z = et; z < nkb * MP; z += 128) {
+                    const int i = z / MP, t = z & (MP - 1);
+                    sxs[z] = t < a.M ? __fmul_rn(a.sxg[static_cast<size_t>(t) * a.kbs + kb0 + i],
+                                                 a.sw[static_cast<size_t>(tile) * a.kbs + kb0 + i])
+                                     : 0.0f;
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+            }
             // (1) Rows M..MP-1 of every block get zero codes and scales (their columns
             // are never stored); chunk z = (i * MP + t) * 8 + ch.
             const int live_rows = a.M;
-            if (live_rows < MP) {
+            if (!a.preq && live_rows < MP) {
                 for (int z = et; z < nkb * MP * 8; z += 128) {
                     const int ch = z & 7, t = (z >> 3) & (MP - 1), i = z / (MP * 8);
                     if (t < live_rows) continue;
@@ -368,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the first MMAs overlap the rest of the quantisation.  sxs holds the block's
             // combined scale sx * sw.
             constexpr int kU = 8;
-            const int groups = nkb * live_rows;
+            const int groups = a.preq ? 0 : nkb * live_rows;
             const int step_i = 16 / live_rows, step_t = 16 % live_rows;
             int gi = (et >> 3) / live_rows, gt = (et >> 3) % live_rows;     // (i, t) of this thread's next group
             int released = 0;
@@ -833,13 +856,24 @@ size_t smem_bytes_a8(int mp, int stages, size_t recv, int xq_blocks)
 
 }  // namespace
 
+size_t a8_workspace_bytes(int M, int K)
+{
+    const size_t nb = static_cast<size_t>((K + kA8Block - 1) / kA8Block);
+    const size_t q = (static_cast<size_t>(M) * K + 255) / 256 * 256;
+    return kWsData + q + (static_cast<size_t>(M) * nb * 4 + 255) / 256 * 256;
+}
+
 dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x, const void* Wq, const float* sw,
                        void* y, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     (void)dev;
     if (M < 1 || M > kA8MaxRows || K % 16 != 0) return DG_ERR_UNSUPPORTED_SHAPE;
-    for (int i = 1; i < 6; ++i)
+    if (c.params[1] != 0 && c.params[1] != 1) return DG_ERR_BAD_VARIANT;
+    for (int i = 2; i < 6; ++i)
         if (c.params[i] != 0) return DG_ERR_BAD_VARIANT;
+    // params[1] = 1: quantise in a launch of its own into the workspace, then stream the
+    // codes by TMA (the same codes, scales and fold: the same bits).
+    const bool preq = c.params[1] == 1;
     const int mp = tc_mp(M);
     const void* fn = tc_lookup(mp, 2);
     if (!fn) return DG_ERR_BAD_VARIANT;
@@ -872,7 +906,9 @@ dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x,
     const size_t per_sm = 228 * 1024;
     const size_t min_smem = per_sm / (512 / (kA8Bufs * mp) + 1) + 1024;
     if (smem < min_smem) smem = min_smem;
-    if (ws_bytes < kWsData) return DG_ERR_WORKSPACE_TOO_SMALL;
+    if (ws_bytes < (preq ? a8_workspace_bytes(M, K) : kWsData)) return DG_ERR_WORKSPACE_TOO_SMALL;
+    uint8_t* qws = static_cast<uint8_t*>(ws) + kWsData;
+    float* sxws = reinterpret_cast<float*>(qws + (static_cast<size_t>(M) * K + 255) / 256 * 256);
     TcArgs a{};
     a.N = N;
     a.K = K;
@@ -891,11 +927,20 @@ dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x,
     a.sw = sw;
     a.kbs = nkb;
     a.xq_blocks = xq_blocks;
-    CUtensorMap tmW;
+    a.preq = preq ? 1 : 0;
+    a.sxg = sxws;
+    CUtensorMap tmW, tmQ;
     if (!encode_2d(&tmW, Wq, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kA8Block, kTileRows, true))
         return DG_ERR_CUDA;
+    if (preq && !encode_2d(&tmQ, qws, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kA8Block,
+                           static_cast<uint32_t>(mp), true))
+        return DG_ERR_CUDA;
     if (occupancy(fn, kThreads, smem) < 1) return DG_ERR_UNSUPPORTED_SHAPE;
-    void* args[] = {&tmW, &tmW, &a};
+    if (preq) {
+        const dg_status st = launch_a8_quant(x, qws, sxws, M, K, stream);
+        if (st != DG_OK) return st;
+    }
+    void* args[] = {&tmW, preq ? &tmQ : &tmW, &a};
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.tiles * a.nsplit));
     cfg.blockDim = dim3(kThreads);

@@ -93,7 +93,9 @@ typedef enum {
  *   DG_VAR_TC:      [0] pipeline stages (0 = derived from the shape); bf16 linear and
  *                   gate/up: [1] K-split rule, 0 = sized by the shape and the row
  *                   count, 1 = by the shape alone (the batch-invariant mode's choice;
- *                   the two agree up to 128 rows)
+ *                   the two agree up to 128 rows); A8W8: [1] 1 = quantise the activations
+ *                   in a launch of its own into the workspace and stream the codes by TMA
+ *                   (0 = the quantisation fused into the tensor-core kernel; same bits)
  * For the MoE ops, params[3] is the N-tile width in rows (0 = derived) and
  * params[4] the most (token, slot) pairs of one expert per pass over its rows
  * (1, 2, 4 or 8; 0 = 2). */
@@ -287,7 +289,8 @@ dg_status dg_moe_w2(const void* a, const int32_t* topk_ids, const float* gw, con
  * per 128 x 128 weight block, row-major), y [M, N] bf16.  1 <= M <= 64, K % 16 == 0.
  * Runs on the tensor cores only (DG_VAR_TC; params[0] pipeline stages); the K-split
  * is fixed by (N, K), so output row m depends on input row m alone at every M.
- * Non-finite activations give NaN outputs for their token.  ws: status word only. */
+ * Non-finite activations give NaN outputs for their token.  ws: the status word, and
+ * the codes and scales when the quantisation runs as a launch of its own. */
 dg_status dg_gemv_a8w8_blockscale(const void* x, const void* Wq, const float* sw, void* y, int M, int N, int K,
                                   void* ws, size_t ws_bytes, dg_stream_t stream, const dg_choice* choice);
 

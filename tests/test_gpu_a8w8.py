@@ -55,12 +55,13 @@ def test_quant_codes_and_scales_bit_exact(cuda_device, M, K, seed):
     assert np.array_equal(sx.cpu().numpy().view(np.uint32), sx_ref.view(np.uint32))
 
 
+@pytest.mark.parametrize("pq", [0, 1])
 @pytest.mark.parametrize("M,N,K", SMALL)
-def test_a8w8_small_exhaustive(cuda_device, M, N, K):
+def test_a8w8_small_exhaustive(cuda_device, M, N, K, pq):
     _, Wq, sw = S.a8w8_inputs(1, N, K, device=cuda_device)
     x = _wide_x(M, K, M + N + K, cuda_device)
     ws = dg.workspace(dg.DG_OP_GEMV_A8W8, M, N, K)
-    y = dg.dg_gemv_a8w8_blockscale(x, Wq, sw, ws=ws)
+    y = dg.dg_gemv_a8w8_blockscale(x, Wq, sw, ws=ws, choice=dg.Choice.make(dg.DG_VAR_TC, 0, pq))
     torch.cuda.synchronize()
     _check(x, Wq, sw, y)
     assert dg.dg_device_status(ws) == 0
@@ -75,17 +76,21 @@ def test_a8w8_full_size_sampled(cuda_device, M, N, K):
     _check(x, Wq, sw, y, rows=sample_rows(N, 96, seed=N + K + M))
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 8192, 4096), (16, 32768, 1024), (40, 700, 2064), (64, 8192, 4096)])
-def test_a8w8_stages_bitwise_identical(cuda_device, M, N, K):
+@pytest.mark.parametrize("M,N,K", [(1, 8192, 4096), (16, 32768, 1024), (40, 700, 2064), (64, 8192, 4096),
+                                   (3, 130, 1040)])
+def test_a8w8_variants_bitwise_identical(cuda_device, M, N, K):
+    """Pipeline depth, and the quantisation fused or run as a launch of its own (codes
+    streamed by TMA), give the same bits."""
     x, Wq, sw = S.a8w8_inputs(M, N, K, device=cuda_device)
     ref = dg.dg_gemv_a8w8_blockscale(x, Wq, sw)
-    for st in range(2, 9):
-        try:
-            y = dg.dg_gemv_a8w8_blockscale(x, Wq, sw, choice=dg.Choice.make(dg.DG_VAR_TC, st))
-        except dg.DGError as e:
-            assert e.status in (3, 8), (st, e.status)
-            continue
-        assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), st
+    for pq in (0, 1):
+        for st in [0] + list(range(2, 9)):
+            try:
+                y = dg.dg_gemv_a8w8_blockscale(x, Wq, sw, choice=dg.Choice.make(dg.DG_VAR_TC, st, pq))
+            except dg.DGError as e:
+                assert e.status in (3, 8), (st, pq, e.status)
+                continue
+            assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), (st, pq)
 
 
 @pytest.mark.parametrize("N,K", [(8192, 4096), (300, 1040)])
