@@ -291,9 +291,10 @@ def run_gpu(args):
                 x = S.normal_bf16((M, K), 1.0, S.seed_for("a8w8", "x", N, K, M), dev)
                 y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
                 ws = dg.workspace(dg.DG_OP_GEMV_A8W8, M, N, K, device=dev)
-                add("gemv_a8w8", {"M": M, "N": N, "K": K},
+                sep = dg.dg_select(dg.DG_OP_GEMV_A8W8, M, N, K).params[1] == 1    # quantisation launch first
+                add("gemv_a8w8", {"M": M, "N": N, "K": K, "quant": "separate launch" if sep else "fused"},
                     [(lambda W=W, x=x, y=y, ws=ws, sw=sw: dg.dg_gemv_a8w8_blockscale(x, W, sw, y, ws=ws, stream=stream))
-                     for W in Wa], wb)
+                     for W in Wa], wb, launches_per_call=2 if sep else 1)
             del Wa
         # --- the bf16 sweep shapes at 1-2 rows in the batch-invariant numerics mode (the
         #     tensor-core family where the fastest mode takes the CUDA cores)

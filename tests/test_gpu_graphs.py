@@ -124,6 +124,25 @@ def test_moe_graph_replay(cuda_device, M, choice):
     assert dg.dg_device_status(ws1) == 0 and dg.dg_device_status(ws2) == 0
 
 
+@pytest.mark.parametrize("pq", [0, 1], ids=["fused", "separate"])
+@pytest.mark.parametrize("M", [1, 24])
+def test_a8w8_graph_replay(cuda_device, M, pq):
+    N, K = 1536, 2048
+    _, Wq, sw = S.a8w8_inputs(1, N, K, device=cuda_device)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GEMV_A8W8, M, N, K)
+    choice = dg.Choice.make(dg.DG_VAR_TC, 0, pq)
+
+    def make(seed):
+        return [S.normal_bf16((M, K), 1.0, 2000 + seed, device=cuda_device)]
+
+    def run(inp):
+        return [dg.dg_gemv_a8w8_blockscale(inp[0], Wq, sw, y=y, ws=ws, choice=choice)]
+
+    _graph_matches_eager(run, make)
+    assert dg.dg_device_status(ws) == 0
+
+
 def test_calls_do_not_synchronise(cuda_device):
     """With preallocated outputs and workspaces no entry point blocks the host."""
     M, N, K = 4, 1024, 1024
@@ -134,8 +153,15 @@ def test_calls_do_not_synchronise(cuda_device):
     _, Wq, scale = S.head_inputs(M, 8192, K, device=cuda_device)
     lg = torch.empty((M, 8192), dtype=torch.bfloat16, device=cuda_device)
     am = torch.empty((M,), dtype=torch.int32, device=cuda_device)
+    _, Wq8, sw = S.a8w8_inputs(M, N, K, device=cuda_device)
+    y8 = torch.empty((M, N), dtype=torch.bfloat16, device=cuda_device)
+    ws8 = dg.workspace(dg.DG_OP_GEMV_A8W8, 32, N, K)
+    x32 = S.normal_bf16((32, K), 1.0, 7, device=cuda_device)
+    y32 = torch.empty((32, N), dtype=torch.bfloat16, device=cuda_device)
     dg.dg_gemv_bf16(x, W, y=y, ws=ws)
     dg.dg_head_fp8_argmax(x, Wq, scale, logits=lg, argmax=am, ws=ws_h)
+    dg.dg_gemv_a8w8_blockscale(x, Wq8, sw, y=y8, ws=ws8)
+    dg.dg_gemv_a8w8_blockscale(x32, Wq8, sw, y=y32, ws=ws8)
     torch.cuda.synchronize()
     prev = torch.cuda.get_sync_debug_mode()
     torch.cuda.set_sync_debug_mode("error")
@@ -143,6 +169,8 @@ def test_calls_do_not_synchronise(cuda_device):
         for _ in range(3):
             dg.dg_gemv_bf16(x, W, y=y, ws=ws)
             dg.dg_head_fp8_argmax(x, Wq, scale, logits=lg, argmax=am, ws=ws_h)
+            dg.dg_gemv_a8w8_blockscale(x, Wq8, sw, y=y8, ws=ws8)
+            dg.dg_gemv_a8w8_blockscale(x32, Wq8, sw, y=y32, ws=ws8)
     finally:
         torch.cuda.set_sync_debug_mode(prev)
     torch.cuda.synchronize()

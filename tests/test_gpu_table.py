@@ -21,6 +21,7 @@ SHAPES = [
     (dg.DG_OP_HEAD_FP8_ARGMAX, 1, 8192, 1024, 0, 0),
     (dg.DG_OP_MOE_W1, 2, 256, 512, 6, 16),
     (dg.DG_OP_MOE_W2, 2, 512, 256, 6, 16),
+    (dg.DG_OP_GEMV_A8W8, 4, 2048, 1024, 0, 0),
 ]
 
 
