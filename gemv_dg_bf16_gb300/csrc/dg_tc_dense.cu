@@ -725,11 +725,13 @@ int tc_nsplit(int N, int K, int M, bool fixed)
 {
     const int tiles = (N + kTileRows - 1) / kTileRows;
     const int nkb = (K + kKB - 1) / kKB;
-    // Up to 128 tokens two CTAs share an SM (about 160 CTAs in all); 256-token tiles
-    // take one SM each, so their split keeps the grid within one wave of 152.  A
+    // Up to 128 tokens two CTAs share an SM: the split fills both slots of every SM
+    // (at most 304 CTAs, one wave; measured on GB300 6-11 % faster than about 160
+    // CTAs on the 64-100 MB shapes, where a few doubled-up SMs set the pace).
+    // 256-token tiles take one SM each, so their split keeps the grid within 152.  A
     // fixed split takes the first rule at every row count, so a row's bits do not
     // depend on how many rows share the call.
-    int ns = (fixed || tc_mp(M) <= 128) ? (160 + tiles - 1) / tiles : 152 / tiles;
+    int ns = (fixed || tc_mp(M) <= 128) ? 304 / tiles : 152 / tiles;
     if (ns > kMaxCluster) ns = kMaxCluster;
     if (ns > nkb) ns = nkb;
     if (ns < 1) ns = 1;
@@ -834,10 +836,10 @@ int tc_a8_nsplit(int N, int K)
 {
     const int tiles = (N + kTileRows - 1) / kTileRows;
     const int nkb = (K + kA8Block - 1) / kA8Block;
-    // About 160 CTAs (two per SM), and at most 8 K-blocks of quantised activations per
-    // rank (64 KB at 64 tokens); a function of the shape alone, so a row's bits do not
-    // depend on how many rows share the call.
-    int ns = (160 + tiles - 1) / tiles;
+    // Both CTA slots of every SM (at most 304 CTAs), and at most 8 K-blocks of quantised
+    // activations per rank (64 KB at 64 tokens); a function of the shape alone, so a
+    // row's bits do not depend on how many rows share the call.
+    int ns = 304 / tiles;
     const int by_smem = (nkb + 7) / 8;
     if (ns < by_smem) ns = by_smem;
     if (ns > kMaxCluster) ns = kMaxCluster;
