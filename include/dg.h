@@ -1,7 +1,7 @@
 /*
  * dg.h -- libdecodegemm: decode-time skinny linear layers on GB300 (sm_103a).
  *
- * One C ABI for the five operations a decode step runs against large weight
+ * One C ABI for the operations a decode step runs against large weight
  * matrices with few token rows (M = 1..128; the bf16 linear and gate/up also
  * take the mid-M range 129..512):
  *
@@ -11,9 +11,14 @@
  *                       greedy (temperature 0) argmax fused into the same launch
  *   dg_moe_w1_silu      routed-expert W1 (gate+up) with SiLU.mul, N-split
  *   dg_moe_w2           routed-expert W2 with the gate-weighted combine, N-split
+ *   dg_gemv_a8w8_blockscale
+ *                       e4m3 weights with 128 x 128 block scales, the per-(token,
+ *                       128-block) activation quantisation fused in (M <= 64)
  *
  * plus dg_select, which maps (op, M, N, K) to a kernel variant through a
- * per-device shape table written by an on-device sweep (dg_sweep).
+ * per-device shape table written by an on-device sweep (dg_sweep), and a
+ * process-wide numerics mode (dg_set_numerics) that can make every row's result
+ * independent of the batch it is computed in.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
