@@ -83,3 +83,29 @@ def test_stale_table_refused_on_device(table, tmp_path, cuda_device):
         dg.dg_table_load(str(bad))
     assert e.value.status == 6
     assert dg.dg_table_entries() == 0
+
+
+def test_batch_invariant_mode_ignores_picks_of_the_other_family(table, cuda_device):
+    """A loaded table's CUDA-core pick (1 row) is not used in the batch-invariant mode;
+    a tensor-core pick (16 rows) is, with the K-split fixed by the shape."""
+    path, doc = table
+    dg.dg_table_load(path)
+    try:
+        assert dg.dg_select(dg.DG_OP_GEMV_BF16, 1, 2048, 1024).from_table == 1
+        dg.dg_set_numerics(dg.DG_NUMERICS_BATCH_INVARIANT)
+        try:
+            c1 = dg.dg_select(dg.DG_OP_GEMV_BF16, 1, 2048, 1024)
+            assert c1.variant == dg.DG_VAR_TC and c1.from_table == 0 and c1.params[1] == 1
+            c16 = dg.dg_select(dg.DG_OP_GEMV_BF16, 16, 4096, 1024)
+            ent = [e for e in doc["entries"] if e["op"] == "gemv_bf16" and e["M"] == 16][0]
+            assert c16.from_table == 1 and c16.variant == ent["pick"]["variant"] == dg.DG_VAR_TC
+            assert c16.params[0] == ent["pick"]["params"][0] and c16.params[1] == 1
+            # the two rows computed through the mode agree with a 16-row call
+            x, W = S.linear_inputs(16, 4096, 1024, device=cuda_device)
+            y16 = dg.dg_gemv_bf16(x, W)
+            y1 = dg.dg_gemv_bf16(x[:1].contiguous(), W)
+            assert torch.equal(y1.view(torch.int16), y16[:1].view(torch.int16))
+        finally:
+            dg.dg_set_numerics(dg.DG_NUMERICS_FASTEST)
+    finally:
+        dg.dg_table_clear()
