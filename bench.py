@@ -129,6 +129,23 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- GPU arm
 
+def _max_over_ranks(x: float, device) -> float:
+    """The largest x over all ranks of the process group (x itself without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_value(world: int, step_bytes: float, step_us: float) -> float:
+    """Whole-job GB/s: every rank (an independent replica) streams step_bytes per step,
+    and the job's step lasts as long as its slowest rank's."""
+    return world * step_bytes / (step_us * 1e-6) / 1e9
+
+
 def _graph_case(torch, calls, reps: int, stream):
     """Capture `reps` calls (a list of closures, used round-robin) into one CUDA graph."""
     for c in calls[:2]:
@@ -428,11 +445,8 @@ def run_gpu(args):
     step_us = sum(s["us"] for s in sweep)
     step_bytes = sum(s["weight_bytes"] for s in sweep)
     value_rank = step_bytes / (step_us * 1e-6) / 1e9
-    if world > 1:
-        t = torch.tensor([step_us], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_us = float(t.item())
-    value = world * step_bytes / (step_us * 1e-6) / 1e9
+    step_us = _max_over_ranks(step_us, dev)
+    value = _job_value(world, step_bytes, step_us)
     small = [s for s in sweep if s["M"] <= 16]
     # Which kernel family the dispatch sends each sweep shape to; the roofline is
     # reported for the family that takes the most time.
