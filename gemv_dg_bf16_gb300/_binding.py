@@ -151,6 +151,27 @@ def _choice(choice):
     return ctypes.byref(Choice.make(*choice))
 
 
+_FP8 = tuple(d for d in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if d is not None)
+
+
+def _expect(t, name, dtypes, shape=None, min_numel=None):
+    """Dtype and shape of a tensor argument.  The C entry points take raw pointers and
+    cannot see sizes, so a mismatch is refused here (ValueError) before any call."""
+    if t is None:
+        return
+    dtypes = dtypes if isinstance(dtypes, tuple) else (dtypes,)
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype}, expected {' or '.join(str(d) for d in dtypes)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if min_numel is not None and t.numel() < min_numel:
+        raise ValueError(f"{name}: {t.numel()} elements, expected at least {min_numel}")
+
+
+def _nbytes(t):
+    return t.numel() * t.element_size()
+
+
 def _check_dev(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -193,6 +214,7 @@ DG_ROUTE_DEBUG_INTS = 2 + 128 + 16 + 128 + 129 + 128 + 128
 
 def dg_moe_route_debug(topk_ids, E: int, ws=None, stream=None) -> dict:
     """The MoE kernels' routing tables for topk_ids [M, topk] (device int32), as numpy."""
+    _expect(topk_ids, "topk_ids", torch.int32)
     _check_dev(topk_ids)
     M, topk = topk_ids.shape
     out = torch.empty(DG_ROUTE_DEBUG_INTS, dtype=torch.int32, device=topk_ids.device)
@@ -241,8 +263,11 @@ def dg_gemv_bf16(x, W, y=None, ws=None, choice=None, stream=None):
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     if ws is None:
         ws = workspace(DG_OP_GEMV_BF16, M, N, K, device=x.device)
+    _expect(x, "x", torch.bfloat16)
+    _expect(W, "W", torch.bfloat16, (N, K))
+    _expect(y, "y", torch.bfloat16, (M, N))
     _check_dev(x, W, y, ws)
-    _ok(lib().dg_gemv_bf16(_ptr(x), _ptr(W), _ptr(y), M, N, K, _ptr(ws), ws.numel(), _stream(stream),
+    _ok(lib().dg_gemv_bf16(_ptr(x), _ptr(W), _ptr(y), M, N, K, _ptr(ws), _nbytes(ws), _stream(stream),
                            _choice(choice)), "dg_gemv_bf16")
     return y
 
@@ -256,8 +281,12 @@ def dg_gemv_a8w8_blockscale(x, Wq, sw, y=None, ws=None, choice=None, stream=None
         y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     if ws is None:
         ws = workspace(DG_OP_GEMV_A8W8, M, N, K, device=x.device)
+    _expect(x, "x", torch.bfloat16)
+    _expect(Wq, "Wq", _FP8, (N, K))
+    _expect(sw, "sw", torch.float32, ((N + 127) // 128, (K + 127) // 128))
+    _expect(y, "y", torch.bfloat16, (M, N))
     _check_dev(x, Wq, sw, y, ws)
-    _ok(lib().dg_gemv_a8w8_blockscale(_ptr(x), _ptr(Wq), _ptr(sw), _ptr(y), M, N, K, _ptr(ws), ws.numel(),
+    _ok(lib().dg_gemv_a8w8_blockscale(_ptr(x), _ptr(Wq), _ptr(sw), _ptr(y), M, N, K, _ptr(ws), _nbytes(ws),
                                       _stream(stream), _choice(choice)), "dg_gemv_a8w8_blockscale")
     return y
 
@@ -269,6 +298,9 @@ def dg_quant_a8_blockscale(x, q=None, sx=None, stream=None):
         q = torch.empty((M, K), dtype=torch.uint8, device=x.device)
     if sx is None:
         sx = torch.empty((M, (K + 127) // 128), dtype=torch.float32, device=x.device)
+    _expect(x, "x", torch.bfloat16)
+    _expect(q, "q", _FP8, (M, K))
+    _expect(sx, "sx", torch.float32, (M, (K + 127) // 128))
     _check_dev(x, q, sx)
     _ok(lib().dg_quant_a8_blockscale(_ptr(x), _ptr(q), _ptr(sx), M, K, _stream(stream)), "dg_quant_a8_blockscale")
     return q, sx
@@ -282,8 +314,11 @@ def dg_gate_up_silu(x, W_gu, out=None, ws=None, choice=None, stream=None):
         out = torch.empty((M, Nh), dtype=torch.bfloat16, device=x.device)
     if ws is None:
         ws = workspace(DG_OP_GATE_UP_SILU, M, Nh, K, device=x.device)
+    _expect(x, "x", torch.bfloat16)
+    _expect(W_gu, "W_gu", torch.bfloat16, (2 * Nh, K))
+    _expect(out, "out", torch.bfloat16, (M, Nh))
     _check_dev(x, W_gu, out, ws)
-    _ok(lib().dg_gate_up_silu(_ptr(x), _ptr(W_gu), _ptr(out), M, Nh, K, _ptr(ws), ws.numel(),
+    _ok(lib().dg_gate_up_silu(_ptr(x), _ptr(W_gu), _ptr(out), M, Nh, K, _ptr(ws), _nbytes(ws),
                               _stream(stream), _choice(choice)), "dg_gate_up_silu")
     return out
 
@@ -299,9 +334,14 @@ def dg_head_fp8_argmax(x, Wq, scale, logits=None, argmax=None, ws=None, choice=N
         argmax = torch.empty((M,), dtype=torch.int32, device=x.device)
     if ws is None:
         ws = workspace(DG_OP_HEAD_FP8_ARGMAX, M, N, K, device=x.device)
+    _expect(x, "x", torch.bfloat16)
+    _expect(Wq, "Wq", _FP8, (N, K))
+    _expect(scale, "scale", torch.float32, min_numel=1)
+    _expect(logits, "logits", torch.bfloat16, (M, N))
+    _expect(argmax, "argmax", torch.int32, (M,))
     _check_dev(x, Wq, scale, logits, argmax, ws)
     _ok(lib().dg_head_fp8_argmax(_ptr(x), _ptr(Wq), _ptr(scale), _ptr(logits), _ptr(argmax), M, N, K,
-                                 _ptr(ws), ws.numel(), _stream(stream), _choice(choice)),
+                                 _ptr(ws), _nbytes(ws), _stream(stream), _choice(choice)),
         "dg_head_fp8_argmax")
     return logits, argmax
 
@@ -315,6 +355,11 @@ def dg_head_fp8_argmax_noalloc(x, Wq, scale, logits=None, argmax=None, choice=No
         logits = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     if argmax is None:
         argmax = torch.empty((M,), dtype=torch.int32, device=x.device)
+    _expect(x, "x", torch.bfloat16)
+    _expect(Wq, "Wq", _FP8, (N, K))
+    _expect(scale, "scale", torch.float32, min_numel=1)
+    _expect(logits, "logits", torch.bfloat16, (M, N))
+    _expect(argmax, "argmax", torch.int32, (M,))
     _check_dev(x, Wq, scale, logits, argmax)
     _ok(lib().dg_head_fp8_argmax_noalloc(_ptr(x), _ptr(Wq), _ptr(scale), _ptr(logits), _ptr(argmax), M, N,
                                          K, _stream(stream), _choice(choice)), "dg_head_fp8_argmax_noalloc")
@@ -331,9 +376,14 @@ def dg_moe_w1_silu(x, topk_ids, W1, s1, a=None, ws=None, choice=None, stream=Non
         a = torch.empty((M, topk, I), dtype=torch.bfloat16, device=x.device)
     if ws is None:
         ws = workspace(DG_OP_MOE_W1, M, I, K, topk, device=x.device)
+    _expect(x, "x", torch.bfloat16)
+    _expect(topk_ids, "topk_ids", torch.int32, (M, topk))
+    _expect(W1, "W1", _FP8, (E, 2 * I, K))
+    _expect(s1, "s1", torch.float32, (E, 2 * I))
+    _expect(a, "a", torch.bfloat16, (M, topk, I))
     _check_dev(x, topk_ids, W1, s1, a, ws)
     _ok(lib().dg_moe_w1_silu(_ptr(x), _ptr(topk_ids), _ptr(W1), _ptr(s1), _ptr(a), M, topk, E, I, K,
-                             _ptr(ws), ws.numel(), _stream(stream), _choice(choice)), "dg_moe_w1_silu")
+                             _ptr(ws), _nbytes(ws), _stream(stream), _choice(choice)), "dg_moe_w1_silu")
     return a
 
 
@@ -345,9 +395,15 @@ def dg_moe_w2(a, topk_ids, topk_w, W2, s2, y=None, ws=None, choice=None, stream=
         y = torch.empty((M, Nout), dtype=torch.bfloat16, device=a.device)
     if ws is None:
         ws = workspace(DG_OP_MOE_W2, M, Nout, I, topk, device=a.device)
+    _expect(a, "a", torch.bfloat16)
+    _expect(topk_ids, "topk_ids", torch.int32, (M, topk))
+    _expect(topk_w, "topk_w", torch.float32, (M, topk))
+    _expect(W2, "W2", _FP8, (E, Nout, I))
+    _expect(s2, "s2", torch.float32, (E, Nout))
+    _expect(y, "y", torch.bfloat16, (M, Nout))
     _check_dev(a, topk_ids, topk_w, W2, s2, y, ws)
     _ok(lib().dg_moe_w2(_ptr(a), _ptr(topk_ids), _ptr(topk_w), _ptr(W2), _ptr(s2), _ptr(y), M, topk, E,
-                        I, Nout, _ptr(ws), ws.numel(), _stream(stream), _choice(choice)), "dg_moe_w2")
+                        I, Nout, _ptr(ws), _nbytes(ws), _stream(stream), _choice(choice)), "dg_moe_w2")
     return y
 
 

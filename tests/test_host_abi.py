@@ -270,3 +270,35 @@ def test_a8w8_table_refuses_cuda_core_pick(tmp_path):
     assert s == 6 and "tensor cores only" in why
     ent = [{"op": "gemv_a8w8", "M": 4, "N": 64, "K": 64, "pick": {"variant": 3, "params": [4]}}]
     assert _check(_table(tmp_path, entries=ent))[0] == 0
+
+
+def test_binding_refuses_mismatched_tensors_before_any_call():
+    """The C entry points see raw pointers only; the binding checks dtypes and shapes
+    first (these CPU tensors never reach the library)."""
+    import torch
+    bf, u8, f32, i32 = torch.bfloat16, torch.uint8, torch.float32, torch.int32
+    x = torch.zeros((2, 256), dtype=bf)
+    cases = [
+        (lambda: dg.dg_gemv_bf16(x, torch.zeros((64, 128), dtype=bf)), "W: shape"),
+        (lambda: dg.dg_gemv_bf16(x, torch.zeros((64, 256), dtype=torch.float16)), "W: dtype"),
+        (lambda: dg.dg_gemv_bf16(x, torch.zeros((64, 256), dtype=bf), y=torch.zeros((2, 63), dtype=bf)), "y: shape"),
+        (lambda: dg.dg_gate_up_silu(x, torch.zeros((63, 256), dtype=bf)), "W_gu: shape"),
+        (lambda: dg.dg_head_fp8_argmax(x, torch.zeros((100, 256), dtype=u8), torch.zeros(1, dtype=torch.float64)),
+         "scale: dtype"),
+        (lambda: dg.dg_head_fp8_argmax(x, torch.zeros((100, 256), dtype=u8), torch.zeros(1, dtype=f32),
+                                       argmax=torch.zeros(2, dtype=torch.int64)), "argmax: dtype"),
+        (lambda: dg.dg_moe_w1_silu(x, torch.zeros((2, 6), dtype=torch.int64), torch.zeros((8, 128, 256), dtype=u8),
+                                   torch.zeros((8, 128), dtype=f32)), "topk_ids: dtype"),
+        (lambda: dg.dg_moe_w1_silu(x, torch.zeros((2, 6), dtype=i32), torch.zeros((8, 128, 256), dtype=u8),
+                                   torch.zeros((8, 64), dtype=f32)), "s1: shape"),
+        (lambda: dg.dg_moe_w2(torch.zeros((2, 6, 64), dtype=bf), torch.zeros((2, 6), dtype=i32),
+                              torch.zeros((2, 5), dtype=f32), torch.zeros((8, 128, 64), dtype=u8),
+                              torch.zeros((8, 128), dtype=f32)), "topk_w: shape"),
+        (lambda: dg.dg_gemv_a8w8_blockscale(x, torch.zeros((300, 256), dtype=u8), torch.zeros((2, 2), dtype=f32)),
+         "sw: shape"),
+        (lambda: dg.dg_quant_a8_blockscale(x, sx=torch.zeros((2, 3), dtype=f32)), "sx: shape"),
+    ]
+    for fn, needle in cases:
+        with pytest.raises(ValueError) as e:
+            fn()
+        assert needle in str(e.value), (needle, str(e.value))
