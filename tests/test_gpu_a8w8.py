@@ -141,3 +141,21 @@ def test_a8w8_graph_replay_and_no_sync(cuda_device):
     torch.cuda.synchronize()
     assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
     assert dg.dg_device_status(ws) == 0
+
+
+def test_a8w8_argument_errors_launch_nothing(cuda_device):
+    x, Wq, sw = S.a8w8_inputs(2, 300, 1040, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GEMV_A8W8, 2, 300, 1040)
+    with pytest.raises(dg.DGError) as e:                     # workspace too small
+        dg.dg_gemv_a8w8_blockscale(x, Wq, sw, ws=ws[:1024])
+    assert e.value.status == dg.DG_ERR_WORKSPACE_TOO_SMALL
+    with pytest.raises(dg.DGError) as e:                     # a CUDA-core variant does not exist here
+        dg.dg_gemv_a8w8_blockscale(x, Wq, sw, choice=dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8))
+    assert e.value.status == dg.DG_ERR_BAD_VARIANT
+    K = 32768                                                # more K-blocks per rank than the kernel holds
+    xl, Wl, swl = S.a8w8_inputs(1, 128, K, device=cuda_device)
+    with pytest.raises(dg.DGError) as e:
+        dg.dg_gemv_a8w8_blockscale(xl, Wl, swl)
+    assert e.value.status == dg.DG_ERR_UNSUPPORTED_SHAPE
+    torch.cuda.synchronize()
+    assert dg.dg_device_status(ws) == 0
