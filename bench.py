@@ -9,7 +9,9 @@ One step = one call of every one of those 40 shapes.
 Metric: microseconds per call and achieved HBM GB/s on weight bytes (fraction of
 the measured HBM peak) per (N,K,M); `value` is the whole step's weight bytes
 divided by its device time (GB/s).  The other hot-path workloads (the bf16 GEMV
-2048x1024 at M=1, fused gate/up, fp8 head + argmax, MoE W1/W2) are measured in the
+2048x1024 at M=1, fused gate/up, fp8 head + argmax, MoE W1/W2, mid-M rows, the A8W8
+block-scaled linear with its activation quantisation, the batch-invariant numerics
+mode at 1-2 rows, and chained gate/up -> down and W1 -> W2 pairs) are measured in the
 same run and reported under "ops".
 
 Timing: each shape's calls are captured in a CUDA graph of R back-to-back calls
