@@ -550,3 +550,18 @@ def test_a8w8_weight_scale_is_linear_exactly():
     y1 = O.a8w8_linear(xb, Wq, sw)["y"]
     y2 = O.a8w8_linear(xb, Wq, (sw * np.float32(2.0)).astype(np.float32))["y"]
     assert np.array_equal(y2, 2.0 * y1)
+
+
+def test_a8_quant_non_finite_reading():
+    """Reading of the pages' silence on non-finite activations: an inf in a block makes
+    that block's scale inf and its codes NaN/zero, so the token's outputs are NaN; the
+    other tokens are untouched.  Saturation maps +-inf inputs of the encoder to +-448."""
+    assert O.e4m3_encode(float("inf")) == 0x7E and O.e4m3_encode(float("-inf")) == 0xFE
+    M, N, K = 2, 130, 256
+    x = torch.ones((M, K))
+    x[0, 3] = float("inf")
+    xb = bf16_bits(x.to(torch.bfloat16))
+    Wq, sw = _a8w8_weights(N, K, 14)
+    r = O.a8w8_linear(xb, Wq, sw)
+    assert np.isinf(r["sx"][0, 0]) and np.isfinite(r["sx"][1]).all()
+    assert np.isnan(r["y"][0]).all() and np.isfinite(r["y"][1]).all()
