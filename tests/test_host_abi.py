@@ -302,3 +302,16 @@ def test_binding_refuses_mismatched_tensors_before_any_call():
         with pytest.raises(ValueError) as e:
             fn()
         assert needle in str(e.value), (needle, str(e.value))
+
+
+def test_binding_op_variant_and_mode_constants_match_header():
+    import re
+    hdr = open(os.path.join(ROOT, "include", "dg.h")).read()
+    enums = dict((k, int(v)) for k, v in re.findall(r"\b(DG_(?:OP|VAR)_\w+)\s*=\s*(\d+)", hdr))
+    defines = dict((k, int(v, 0)) for k, v in re.findall(r"#define\s+(DG_(?:NUMERICS|LAUNCH)_\w+)\s+(0x[0-9A-Fa-f]+|\d+)", hdr))
+    assert {"DG_OP_GEMV_A8W8", "DG_OP_COUNT", "DG_VAR_TC"} <= set(enums)
+    assert {"DG_NUMERICS_FASTEST", "DG_NUMERICS_BATCH_INVARIANT", "DG_LAUNCH_PDL"} <= set(defines)
+    for name, val in {**enums, **defines}.items():
+        if name == "DG_OP_COUNT":
+            continue
+        assert getattr(dg, name) == val, name
