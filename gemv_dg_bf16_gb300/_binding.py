@@ -7,6 +7,7 @@ are torch.bfloat16, e4m3 tensors are torch.uint8 (or float8_e4m3fn) codes.
 from __future__ import annotations
 
 import ctypes
+import json
 import os
 import re
 
@@ -25,7 +26,8 @@ DG_DEVERR_WAIT_TIMEOUT = 0x2
 
 def _rows_buckets():
     with open(os.path.join(_HERE, "csrc", "dg_rows.h")) as f:
-        m = re.search(r"#define DG_ROWS_BUCKETS\(X\)\s+(.*)", f.read())
+        text = f.read().replace("\\\n", " ")          # the macro continues over several lines
+        m = re.search(r"#define DG_ROWS_BUCKETS\(X\)\s+(.*)", text)
     return tuple(int(v) for v in re.findall(r"X\((\d+)\)", m.group(1)))
 
 
@@ -442,7 +444,77 @@ def dg_table_check(path: str, arch: str, driver_version: int, runtime_version: i
     return int(s), int(n.value), buf.value.decode()
 
 
-def dg_sweep(shapes, out_path: str, reps: int = 20):
-    """shapes: iterable of (op, M, N, K, topk[, E]); writes the shape table JSON to out_path."""
+_OP_NAMES = ("gemv_bf16", "gate_up_silu", "head_fp8_argmax", "moe_w1_silu", "moe_w2", "gemv_a8w8")
+
+
+def _bucket(M: int) -> int:
+    for b in ROWS_BUCKETS:
+        if b >= M:
+            return b
+    return -1
+
+
+def _table_key(op_name: str, M: int, N: int, K: int):
+    return (op_name, int(M), int(N), int(K))
+
+
+def _sweep_remaining(shapes, doc):
+    """The shapes whose (op, row bucket, N, K) entry a partial table does not hold yet."""
+    have = {_table_key(e["op"], e["M"], e["N"], e["K"]) for e in doc.get("entries", [])}
+    return [s for s in shapes if _table_key(_OP_NAMES[s[0]], _bucket(s[1]), s[2], s[3]) not in have]
+
+
+def _merge_tables(old, new):
+    """new's identity; old's entries that new does not re-measure, then new's."""
+    fresh = {_table_key(e["op"], e["M"], e["N"], e["K"]) for e in new.get("entries", [])}
+    kept = [e for e in old.get("entries", []) if _table_key(e["op"], e["M"], e["N"], e["K"]) not in fresh]
+    out = dict(new)
+    out["entries"] = kept + list(new.get("entries", []))
+    return out
+
+
+def _sweep_once(shapes, out_path, reps):
     arr = (Shape * len(shapes))(*[Shape(*s) for s in shapes])
     _ok(lib().dg_sweep(arr, len(shapes), out_path.encode(), reps), "dg_sweep")
+
+
+def dg_sweep(shapes, out_path: str, reps: int = 20, resume: bool = False):
+    """shapes: iterable of (op, M, N, K, topk[, E]); writes the shape table JSON to out_path.
+
+    resume=True continues an interrupted sweep: when out_path already holds a table of
+    this build and device (the same identity the new measurements get), its entries are
+    kept and only the missing (op, row bucket, N, K) keys are measured; the merged table
+    then replaces the file in one rename.  Any other file is measured over from scratch."""
+    shapes = [tuple(s) for s in shapes]
+    old = None
+    if resume and os.path.exists(out_path):
+        try:
+            with open(out_path) as f:
+                old = json.load(f)
+        except (OSError, ValueError):
+            old = None
+        if not (isinstance(old, dict) and old.get("format") == "libdecodegemm-table"
+                and old.get("identity", {}).get("build") == dg_build_id()
+                and old.get("identity", {}).get("selection_space") == dg_selection_space()):
+            old = None
+    if old is None:
+        _sweep_once(shapes, out_path, reps)
+        return
+    todo = _sweep_remaining(shapes, old)
+    if not todo:
+        return
+    part = out_path + f".part{os.getpid()}"
+    try:
+        _sweep_once(todo, part, reps)
+        with open(part) as f:
+            new = json.load(f)
+    finally:
+        if os.path.exists(part):
+            os.remove(part)
+    if new.get("identity") != old.get("identity"):      # another device or driver: start over
+        _sweep_once(shapes, out_path, reps)
+        return
+    tmp = out_path + f".tmp{os.getpid()}"
+    with open(tmp, "w") as f:
+        json.dump(_merge_tables(old, new), f, indent=1)
+    os.replace(tmp, out_path)

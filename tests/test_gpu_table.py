@@ -109,3 +109,27 @@ def test_batch_invariant_mode_ignores_picks_of_the_other_family(table, cuda_devi
             dg.dg_set_numerics(dg.DG_NUMERICS_FASTEST)
     finally:
         dg.dg_table_clear()
+
+
+def test_sweep_resumes_a_partial_table(tmp_path, cuda_device):
+    """An interrupted sweep (here: only the first half of the shapes written) continues
+    where it stopped: the finished entries stay as they are, the rest are measured."""
+    path = str(tmp_path / "partial.json")
+    half = SHAPES[:3]
+    dg.dg_sweep(half, path, reps=3)
+    with open(path) as f:
+        first = json.load(f)
+    dg.dg_sweep(SHAPES, path, reps=3, resume=True)
+    with open(path) as f:
+        done = json.load(f)
+    assert len(done["entries"]) == len(SHAPES)
+    assert done["entries"][:3] == first["entries"]
+    assert done["identity"] == first["identity"]
+    dg.dg_table_load(path)                       # the merged table passes the identity checks
+    try:
+        assert dg.dg_table_entries() == len(SHAPES)
+    finally:
+        dg.dg_table_clear()
+    before = open(path).read()
+    dg.dg_sweep(SHAPES, path, reps=3, resume=True)    # nothing left to measure
+    assert open(path).read() == before

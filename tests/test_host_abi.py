@@ -34,7 +34,7 @@ def test_library_has_no_oracle_dependency():
 
 
 def test_rows_buckets_one_list():
-    assert dg.ROWS_BUCKETS == (1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128)
+    assert dg.ROWS_BUCKETS == (1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64, 96, 128, 192, 256, 384, 512)
 
 
 def test_status_strings():
@@ -315,3 +315,25 @@ def test_binding_op_variant_and_mode_constants_match_header():
         if name == "DG_OP_COUNT":
             continue
         assert getattr(dg, name) == val, name
+
+
+def test_sweep_resume_keys_and_merge():
+    """Resuming a sweep measures only the (op, row bucket, N, K) keys a partial table
+    lacks, and the merge keeps the old entries beside the new ones."""
+    from gemv_dg_bf16_gb300 import _binding as Bd
+    old = {"format": "libdecodegemm-table", "identity": {"build": "b1"},
+           "entries": [{"op": "gemv_bf16", "M": 16, "N": 4096, "K": 1024, "pick_us": 5.0},
+                       {"op": "moe_w2", "M": 2, "N": 512, "K": 256, "pick_us": 9.0}]}
+    shapes = [(dg.DG_OP_GEMV_BF16, 13, 4096, 1024, 0, 0),      # bucket 16: already there
+              (dg.DG_OP_GEMV_BF16, 17, 4096, 1024, 0, 0),      # bucket 24: missing
+              (dg.DG_OP_MOE_W2, 2, 512, 256, 6, 16),           # there
+              (dg.DG_OP_GEMV_A8W8, 300, 2048, 1024, 0, 0)]     # bucket 384: missing
+    todo = Bd._sweep_remaining(shapes, old)
+    assert todo == [shapes[1], shapes[3]]
+    new = {"format": "libdecodegemm-table", "identity": {"build": "b1"},
+           "entries": [{"op": "gemv_bf16", "M": 24, "N": 4096, "K": 1024, "pick_us": 6.0},
+                       {"op": "moe_w2", "M": 2, "N": 512, "K": 256, "pick_us": 8.0}]}
+    m = Bd._merge_tables(old, new)
+    keys = [(e["op"], e["M"], e["pick_us"]) for e in m["entries"]]
+    assert keys == [("gemv_bf16", 16, 5.0), ("gemv_bf16", 24, 6.0), ("moe_w2", 2, 8.0)]
+    assert m["identity"] == new["identity"] and Bd._bucket(513) == -1
