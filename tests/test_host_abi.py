@@ -337,3 +337,20 @@ def test_sweep_resume_keys_and_merge():
     keys = [(e["op"], e["M"], e["pick_us"]) for e in m["entries"]]
     assert keys == [("gemv_bf16", 16, 5.0), ("gemv_bf16", 24, 6.0), ("moe_w2", 2, 8.0)]
     assert m["identity"] == new["identity"] and Bd._bucket(513) == -1
+
+
+def test_table_accepts_mid_m_buckets_only(tmp_path):
+    ent = lambda M: [{"op": "gemv_bf16", "M": M, "N": 4096, "K": 1024, "pick": {"variant": 3, "params": [4]}}]
+    for M in (192, 256, 384, 512):
+        assert _check(_table(tmp_path, entries=ent(M)))[0] == 0, M
+    for M in (200, 513, 1024):
+        s, _, why = _check(_table(tmp_path, entries=ent(M)))
+        assert s == 6 and "not a decode bucket" in why, (M, why)
+
+
+def test_select_pads_every_row_count_to_its_bucket():
+    """Every M maps to the default of its bucket (the smallest listed bucket >= M)."""
+    for M in range(1, 513):
+        b = next(r for r in dg.ROWS_BUCKETS if r >= M)
+        assert dg.dg_select(dg.DG_OP_GEMV_BF16, M, 4096, 4096).as_tuple() == \
+            dg.dg_select(dg.DG_OP_GEMV_BF16, b, 4096, 4096).as_tuple(), M
