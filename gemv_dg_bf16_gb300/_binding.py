@@ -103,6 +103,8 @@ def lib():
     L.dg_gate_up_silu.argtypes = [P, P, P, I, I, I, P, Z, P, P]
     L.dg_head_fp8_argmax.argtypes = [P, P, P, P, P, I, I, I, P, Z, P, P]
     L.dg_head_fp8_argmax_noalloc.argtypes = [P, P, P, P, P, I, I, I, P, P]
+    L.dg_head_fp8_argmax_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int32), P]
+    L.dg_head_fp8_argmax_noalloc_scratch.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
     L.dg_moe_w1_silu.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
     L.dg_moe_w2.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, Z, P, P]
     L.dg_gemv_a8w8_blockscale.argtypes = [P, P, P, P, I, I, I, P, Z, P, P]
@@ -119,7 +121,9 @@ def lib():
                                  ctypes.c_char_p, Z]
     L.dg_sweep.argtypes = [ctypes.POINTER(Shape), I, ctypes.c_char_p, I]
     for name in ("dg_init", "dg_device_status", "dg_device_status_clear", "dg_gemv_bf16",
-                 "dg_gate_up_silu", "dg_head_fp8_argmax", "dg_head_fp8_argmax_noalloc", "dg_moe_w1_silu", "dg_moe_w2", "dg_select",
+                 "dg_gate_up_silu", "dg_head_fp8_argmax", "dg_head_fp8_argmax_noalloc",
+                 "dg_head_fp8_argmax_noalloc_status", "dg_head_fp8_argmax_noalloc_scratch", "dg_moe_w1_silu",
+                 "dg_moe_w2", "dg_select",
                  "dg_gemv_a8w8_blockscale", "dg_quant_a8_blockscale",
                  "dg_table_load", "dg_table_check", "dg_sweep"):
         getattr(L, name).restype = S
@@ -366,6 +370,21 @@ def dg_head_fp8_argmax_noalloc(x, Wq, scale, logits=None, argmax=None, choice=No
     _ok(lib().dg_head_fp8_argmax_noalloc(_ptr(x), _ptr(Wq), _ptr(scale), _ptr(logits), _ptr(argmax), M, N,
                                          K, _stream(stream), _choice(choice)), "dg_head_fp8_argmax_noalloc")
     return logits, argmax
+
+
+def dg_head_fp8_argmax_noalloc_status(stream=None) -> int:
+    """The no-allocation head's status word (its latest call); synchronises the stream."""
+    v = ctypes.c_int32(0)
+    _ok(lib().dg_head_fp8_argmax_noalloc_status(ctypes.byref(v), _stream(stream)),
+        "dg_head_fp8_argmax_noalloc_status")
+    return int(v.value)
+
+
+def dg_head_fp8_argmax_noalloc_scratch() -> int:
+    """Device address of the no-allocation head's static scratch on the current device."""
+    p = ctypes.c_void_p(0)
+    _ok(lib().dg_head_fp8_argmax_noalloc_scratch(ctypes.byref(p)), "dg_head_fp8_argmax_noalloc_scratch")
+    return int(p.value)
 
 
 def dg_moe_w1_silu(x, topk_ids, W1, s1, a=None, ws=None, choice=None, stream=None):

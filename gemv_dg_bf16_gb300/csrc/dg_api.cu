@@ -56,9 +56,17 @@ std::atomic<int> g_launch_flags{DG_LAUNCH_PDL};
 
 bool pdl_enabled() { return (g_launch_flags.load(std::memory_order_relaxed) & DG_LAUNCH_PDL) != 0; }
 
+namespace {
+thread_local int t_check_only = 0;
+}
+
+CheckOnly::CheckOnly() { ++t_check_only; }
+CheckOnly::~CheckOnly() { --t_check_only; }
+
 cudaError_t launch_kernel(const void* fn, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
                           void** args)
 {
+    if (t_check_only) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
@@ -246,9 +254,6 @@ const char* dg_status_str(dg_status s)
     }
 }
 
-// Upper bound on the grid of any persistent dense launch (CTA partials of the head).
-static constexpr int kMaxGrid = 4096;
-
 size_t dg_workspace_bytes(dg_op op, int M, int N, int K, int topk)
 {
     (void)K;
@@ -261,7 +266,7 @@ size_t dg_workspace_bytes(dg_op op, int M, int N, int K, int topk)
         if (M > 0 && N > 0 && K > 0) b = tc_workspace_bytes(M, 2 * N, K);
         break;
     case DG_OP_HEAD_FP8_ARGMAX:
-        b += static_cast<size_t>(kMaxGrid) * 8 * 8;
+        b += kHeadPartialBytes;
         break;
     case DG_OP_MOE_W2:
         if (M > 0 && topk > 0 && N > 0) b += moe_terms_bytes(M, topk, N);

@@ -82,6 +82,23 @@ bool pdl_enabled();
 cudaError_t launch_kernel(const void* fn, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
                           void** args);
 
+// While an instance lives, launch_kernel on this thread checks nothing more and
+// launches nothing (returns success): an entry point run under it performs every
+// argument, shape, variant and workspace check of a real call -- the same code --
+// and queues no work.
+struct CheckOnly {
+    CheckOnly();
+    ~CheckOnly();
+    CheckOnly(const CheckOnly&) = delete;
+    CheckOnly& operator=(const CheckOnly&) = delete;
+};
+
+// Upper bound on the grid of any persistent launch of the head, and the bytes of its
+// per-CTA (value, index) partials for 8 rows beyond the workspace header -- the one
+// constant the workspace size and the no-allocation scratch are both built from.
+constexpr int kMaxGrid = 4096;
+constexpr size_t kHeadPartialBytes = static_cast<size_t>(kMaxGrid) * 8 * 8;
+
 // Maximum dynamic shared memory any launch of this library asks for.
 constexpr size_t kMaxDynSmem = 200 * 1024;
 // Budget for staged activations of the dense CUDA-core family.

@@ -245,15 +245,30 @@ dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, 
  * - Arguments and results as dg_head_fp8_argmax, without ws / ws_bytes.
  * - The first call on a device looks up the array's device address (with that
  *   device current); make that first call before any stream capture.
- * - Each call clears the status word and ticket with an asynchronous memset on
- *   `stream`, then launches.
+ * - Every check of the call runs first (the same code as dg_head_fp8_argmax): a
+ *   refused call queues nothing.  An accepted call clears the status word and ticket
+ *   with an asynchronous memset on `stream`, then launches.
  * - All calls share the one array: calls that may overlap on the GPU (different
  *   streams, or different host threads) race and must be serialised by the caller.
- * - A launch that would need more than 4096 CTA partial slots (e.g. a choice with
- *   tiny CTAs) is rejected with DG_ERR_WORKSPACE_TOO_SMALL and one stderr line. */
+ *   The status word therefore describes the latest call only; read it with
+ *   dg_head_fp8_argmax_noalloc_status before the next call clears it.
+ * - A launch that would need more than 4096 CTA partial slots is rejected with
+ *   DG_ERR_WORKSPACE_TOO_SMALL and one stderr line (no grid this library launches for
+ *   the head on a 152-SM part comes near it). */
 dg_status dg_head_fp8_argmax_noalloc(const void* x, const void* Wq, const float* scale, void* logits,
                                      int32_t* argmax, int M, int N, int K, dg_stream_t stream,
                                      const dg_choice* choice);
+
+/* The device status word of the no-allocation head's static scratch, i.e. of its
+ * latest call (DG_DEVERR_* bits; a bounded wait that gave up shows as
+ * DG_DEVERR_WAIT_TIMEOUT): copied to *host_out after synchronising `stream`.  For
+ * health checks, like dg_device_status (no counterpart on the pages). */
+dg_status dg_head_fp8_argmax_noalloc_status(int32_t* host_out, dg_stream_t stream);
+
+/* The static scratch's device address on the current device (a health-check hook,
+ * e.g. to run dg_selftest_wait_timeout on it; no counterpart on the pages).  Looks
+ * the address up on first use, like the first call of the no-allocation head. */
+dg_status dg_head_fp8_argmax_noalloc_scratch(void** device_ptr);
 
 /* Routed-expert W1 with SiLU.mul, "Decode optimization round 3", "Retained
  * change 1: N-split W1/W2 MoE kernels" (experts split along N at small M).

@@ -13,7 +13,7 @@ import gemv_dg_bf16_gb300 as dg
 from oracle import oracle as O
 from oracle import tolerance as T
 from synth import decode_inputs as S
-from tests._helpers import bits16, f64, sample_rows
+from tests._helpers import bits16, f64, sample_rows, lin_excess, silu_excess
 
 pytestmark = pytest.mark.gpu
 
@@ -41,7 +41,7 @@ def _wide_x(M, K, seed, device):
 def _check(x, Wq, sw, y, rows=None):
     r = O.a8w8_linear(bits16(x), Wq.cpu().numpy(), sw.cpu().numpy(), rows=rows)
     got = f64(y if rows is None else y[:, torch.as_tensor(rows, device=y.device)])
-    exc = T.linear_excess(got, r["y"], r["absdot"])
+    exc = lin_excess(got, r["y"], r["absdot"])
     assert (exc <= 0).all(), f"max excess {exc.max():.3e} at {np.unravel_index(exc.argmax(), exc.shape)}"
 
 

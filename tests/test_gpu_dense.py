@@ -9,7 +9,7 @@ import gemv_dg_bf16_gb300 as dg
 from oracle import oracle as O
 from oracle import tolerance as T
 from synth import decode_inputs as S
-from tests._helpers import bits16, f64, sample_rows
+from tests._helpers import bits16, f64, sample_rows, lin_excess, silu_excess
 
 pytestmark = pytest.mark.gpu
 
@@ -23,7 +23,7 @@ def _lin_check(x, W, y, rows=None):
     Wb = bits16(W if rows is None else W[torch.as_tensor(rows, device=W.device)])
     ref, ad = O.linear_bf16(xb, Wb)
     got = f64(y if rows is None else y[:, torch.as_tensor(rows, device=y.device)])
-    exc = T.linear_excess(got, ref, ad)
+    exc = lin_excess(got, ref, ad)
     assert (exc <= 0).all(), f"max excess {exc.max():.3e} at {np.unravel_index(exc.argmax(), exc.shape)}"
 
 
@@ -142,7 +142,7 @@ def _gate_up_check(x, Wgu, out, cols=None):
         rows = torch.stack((2 * c, 2 * c + 1), dim=1).reshape(-1)
         r = O.gate_up_silu(bits16(x), bits16(Wgu[rows]))
         got = f64(out[:, c])
-    exc = T.silu_mul_excess(got, r["g"], r["u"], r["absg"], r["absu"], r["out"])
+    exc = silu_excess(got, r["g"], r["u"], r["absg"], r["absu"], r["out"])
     assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
 
 

@@ -8,7 +8,7 @@ import gemv_dg_bf16_gb300 as dg
 from oracle import oracle as O
 from oracle import tolerance as T
 from synth import decode_inputs as S
-from tests._helpers import bits16, f64
+from tests._helpers import bits16, f64, lin_excess, silu_excess
 
 pytestmark = pytest.mark.gpu
 
@@ -27,7 +27,7 @@ def test_wait_timeout_sets_status_and_context_survives(cuda_device):
         y = dg.dg_gemv_bf16(x, W, ws=dg.workspace(dg.DG_OP_GEMV_BF16, 4, 640, 2048), choice=choice)
         torch.cuda.synchronize()
         ref, ad = O.linear_bf16(bits16(x), bits16(W))
-        assert (T.linear_excess(f64(y), ref, ad) <= 0).all()
+        assert (lin_excess(f64(y), ref, ad) <= 0).all()
 
 
 def test_wait_timeout_argument_checks(cuda_device):

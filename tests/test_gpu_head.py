@@ -7,7 +7,7 @@ import gemv_dg_bf16_gb300 as dg
 from oracle import oracle as O
 from oracle import tolerance as T
 from synth import decode_inputs as S
-from tests._helpers import bits16, f64, sample_rows
+from tests._helpers import bits16, f64, sample_rows, lin_excess, silu_excess
 
 pytestmark = pytest.mark.gpu
 
@@ -19,7 +19,7 @@ def _check_logits(x, Wq, scale, logits, rows=None):
     Wn = (Wq if rows is None else Wq[torch.as_tensor(rows, device=Wq.device)]).cpu().numpy()
     lg, ad = O.head_fp8(bits16(x), Wn, sc)
     got = f64(logits if rows is None else logits[:, torch.as_tensor(rows, device=logits.device)])
-    exc = T.linear_excess(got, lg, ad)
+    exc = lin_excess(got, lg, ad)
     assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
 
 

@@ -14,7 +14,7 @@ import gemv_dg_bf16_gb300 as dg
 from oracle import oracle as O
 from oracle import tolerance as T
 from synth import decode_inputs as S
-from tests._helpers import bits16, f64, sample_rows
+from tests._helpers import bits16, f64, sample_rows, lin_excess, silu_excess
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,7 @@ def test_linear_rows_independent_of_the_batch(cuda_device, N, K):
     ci = torch.as_tensor(cols, device=cuda_device)
     ref, ad = O.linear_bf16(bits16(x[:1]), bits16(W[ci]))
     y1 = dg.dg_gemv_bf16(x[:1].contiguous(), W)
-    assert (T.linear_excess(f64(y1[:, ci]), ref, ad) <= 0).all()
+    assert (lin_excess(f64(y1[:, ci]), ref, ad) <= 0).all()
 
 
 @pytest.mark.parametrize("Nh,K", [(700, 4096), (12288, 4096), (96, 1544)])
@@ -64,7 +64,7 @@ def test_gate_up_rows_independent_of_the_batch(cuda_device, Nh, K):
     rows = torch.stack((2 * c, 2 * c + 1), dim=1).reshape(-1)
     r = O.gate_up_silu(bits16(x[:1]), bits16(Wgu[rows]))
     out1 = dg.dg_gate_up_silu(x[:1].contiguous(), Wgu)
-    exc = T.silu_mul_excess(f64(out1[:, c]), r["g"], r["u"], r["absg"], r["absu"], r["out"])
+    exc = silu_excess(f64(out1[:, c]), r["g"], r["u"], r["absg"], r["absu"], r["out"])
     assert (exc <= 0).all()
 
 
@@ -82,7 +82,7 @@ def test_head_rows_and_picks_independent_of_the_batch(cuda_device, N, K, top):
     rows = sample_rows(N, 64, seed=N)
     ri = torch.as_tensor(rows, device=cuda_device)
     ref, ad = O.head_fp8(bits16(x[:1]), Wq[ri].cpu().numpy(), float(scale.cpu()[0]))
-    assert (T.linear_excess(f64(lg8[:1, ri]), ref, ad) <= 0).all()
+    assert (lin_excess(f64(lg8[:1, ri]), ref, ad) <= 0).all()
 
 
 @pytest.mark.parametrize("E,I,K,Nout", [(128, 1536, 4096, 4096), (24, 192, 528, 200)])

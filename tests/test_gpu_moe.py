@@ -7,7 +7,7 @@ import gemv_dg_bf16_gb300 as dg
 from oracle import oracle as O
 from oracle import tolerance as T
 from synth import decode_inputs as S
-from tests._helpers import bits16, f64
+from tests._helpers import bits16, f64, lin_excess, silu_excess
 
 pytestmark = pytest.mark.gpu
 
@@ -52,7 +52,7 @@ def test_moe_w1_full_size(cuda_device, moe_w, M, family):
     a = dg.dg_moe_w1_silu(x, ids, W1q, s1, ws=ws, choice=FAMILIES[family])
     torch.cuda.synchronize()
     r = _w1_ref(x, ids, W1q, s1)
-    exc = T.silu_mul_excess(f64(a), r["g"], r["u"], r["absg"], r["absu"], r["a"])
+    exc = silu_excess(f64(a), r["g"], r["u"], r["absg"], r["absu"], r["a"])
     assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
     assert dg.dg_device_status(ws) == 0
 
@@ -68,7 +68,7 @@ def test_moe_w2_full_size_on_gpu_activations(cuda_device, moe_w, M, family):
     y = dg.dg_moe_w2(a, ids, gw, W2q, s2, ws=ws, choice=c)
     torch.cuda.synchronize()
     ref, bound = _w2_ref(a, ids, gw, W2q, s2)
-    exc = T.linear_excess(f64(y), ref, bound)
+    exc = lin_excess(f64(y), ref, bound)
     assert (exc <= 0).all(), f"max excess {exc.max():.3e}"
     # repeated calls reuse the workspace tickets and give the same bits
     for _ in range(3):
@@ -132,7 +132,7 @@ def test_moe_invalid_ids_flag_and_zero(cuda_device, moe_w, family):
     ids_c = np.array([[remap.get(int(e), -1) for e in row] for row in ids_np], np.int32)
     sel = torch.as_tensor(used, device=cuda_device)
     ref, bound = O.moe_w2(bits16(a), ids_c, gw.cpu().numpy(), W2q[sel].cpu().numpy(), s2[sel].cpu().numpy())
-    exc = T.linear_excess(f64(y), ref, bound)
+    exc = lin_excess(f64(y), ref, bound)
     assert (exc <= 0).all()
 
 
@@ -148,10 +148,10 @@ def test_moe_many_pairs_on_one_expert(cuda_device):
         y = dg.dg_moe_w2(a, ids, gw, W2q, s2, choice=c)
         torch.cuda.synchronize()
         r = O.moe_w1_silu(bits16(x), ids.cpu().numpy(), W1q.cpu().numpy(), s1.cpu().numpy())
-        exc = T.silu_mul_excess(f64(a), r["g"], r["u"], r["absg"], r["absu"], r["a"])
+        exc = silu_excess(f64(a), r["g"], r["u"], r["absg"], r["absu"], r["a"])
         assert (exc <= 0).all(), mt
         ref, bound = O.moe_w2(bits16(a), ids.cpu().numpy(), gw.cpu().numpy(), W2q.cpu().numpy(), s2.cpu().numpy())
-        assert (T.linear_excess(f64(y), ref, bound) <= 0).all(), mt
+        assert (lin_excess(f64(y), ref, bound) <= 0).all(), mt
 
 
 @pytest.mark.parametrize("family", ["cc", "tc"])
@@ -177,7 +177,7 @@ def test_moe_single_expert_equals_scaled_gemv(cuda_device, family):
     torch.cuda.synchronize()
     lg, ad = O.head_fp8(bits16(a[0]), W2q[2].cpu().numpy(), 1.0)
     s = s2[2].cpu().numpy().astype(np.float64)
-    exc = T.linear_excess(f64(y), lg * s, ad * s)
+    exc = lin_excess(f64(y), lg * s, ad * s)
     assert (exc <= 0).all()
 
 
