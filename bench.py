@@ -453,7 +453,7 @@ def run_gpu(args):
     # Which kernel family the dispatch sends each sweep shape to; the roofline is
     # reported for the family that takes the most time.
     fam_names = {dg.DG_VAR_CC_WARP: "cc_dense_kernel", dg.DG_VAR_CC_BULK: "cc_bulk_kernel",
-                 dg.DG_VAR_TC: "tc_dense_kernel"}
+                 dg.DG_VAR_TC: "tc_dense_kernel", dg.DG_VAR_MMA: "mw_dense_kernel"}
     by_kernel = {}
     for s_ in sweep:
         v = dg.dg_select(dg.DG_OP_GEMV_BF16, s_["M"], s_["N"], s_["K"]).variant if s_["op"] == "gemv_bf16" else -1

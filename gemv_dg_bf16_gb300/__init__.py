@@ -8,7 +8,7 @@ missing (there is no CPU fallback).
 from ._binding import (  # noqa: F401
     DG_OP_GATE_UP_SILU, DG_OP_GEMV_BF16, DG_OP_HEAD_FP8_ARGMAX, DG_OP_MOE_W1, DG_OP_MOE_W2, DG_OP_GEMV_A8W8,
     dg_gemv_a8w8_blockscale, dg_quant_a8_blockscale,
-    DG_VAR_CC_BULK, DG_VAR_CC_WARP, DG_VAR_DEFAULT, DG_VAR_TC, DGError,
+    DG_VAR_CC_BULK, DG_VAR_CC_WARP, DG_VAR_DEFAULT, DG_VAR_MMA, DG_VAR_TC, DGError,
     DG_OK, DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_UNSUPPORTED_SHAPE, DG_ERR_WORKSPACE_TOO_SMALL, DG_ERR_CUDA,
     DG_ERR_TABLE_REFUSED, DG_ERR_NO_DEVICE, DG_ERR_BAD_VARIANT, DG_DEVERR_BAD_TOPK_ID, DG_DEVERR_WAIT_TIMEOUT, ROWS_BUCKETS, Choice,
     dg_build_id, dg_device_status, dg_device_status_clear, dg_gate_up_silu, dg_gemv_bf16, dg_head_fp8_argmax,

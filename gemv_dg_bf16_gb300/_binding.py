@@ -17,7 +17,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIBPATH = os.path.join(_HERE, "libdecodegemm.so")
 
 DG_OP_GEMV_BF16, DG_OP_GATE_UP_SILU, DG_OP_HEAD_FP8_ARGMAX, DG_OP_MOE_W1, DG_OP_MOE_W2, DG_OP_GEMV_A8W8 = range(6)
-DG_VAR_DEFAULT, DG_VAR_CC_WARP, DG_VAR_CC_BULK, DG_VAR_TC = range(4)
+DG_VAR_DEFAULT, DG_VAR_CC_WARP, DG_VAR_CC_BULK, DG_VAR_TC, DG_VAR_MMA = range(5)
 (DG_OK, DG_ERR_INVALID_ARG, DG_ERR_ALIGNMENT, DG_ERR_UNSUPPORTED_SHAPE, DG_ERR_WORKSPACE_TOO_SMALL, DG_ERR_CUDA,
  DG_ERR_TABLE_REFUSED, DG_ERR_NO_DEVICE, DG_ERR_BAD_VARIANT) = range(9)
 DG_DEVERR_BAD_TOPK_ID = 0x1

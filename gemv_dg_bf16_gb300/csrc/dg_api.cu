@@ -106,8 +106,13 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
     switch (op) {
     case DG_OP_GEMV_BF16:
     case DG_OP_GATE_UP_SILU: {
-        if (M >= kTcMinRows) {
-            out->variant = DG_VAR_TC;      // dense enough for the tensor cores
+        const bool lin = op == DG_OP_GEMV_BF16;
+        if (M >= kTcMinRows || M > (lin ? kMwMaxRowsLinear : kMwMaxRowsGateUp)) {
+            out->variant = DG_VAR_TC;      // a real dense contraction: tcgen05 tiles
+            break;
+        }
+        if (M >= (lin ? kMwMinRowsLinear : kMwMinRowsGateUp)) {
+            out->variant = DG_VAR_MMA;     // warp-level tensor cores, geometry derived at launch
             break;
         }
         // Rows per warp [0], warps per CTA [1] and K-split warps [3] as dg_sweep
@@ -462,6 +467,7 @@ dg_status dg_gemv_bf16(const void* x, const void* W, void* y, int M, int N, int 
     if ((s = resolve_choice(DG_OP_GEMV_BF16, M, N, K, choice, &c)) != DG_OK) return s;
     if (c.variant == DG_VAR_TC)
         return launch_tc(false, dev, c, x, W, y, M, N, K, N, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    if (c.variant == DG_VAR_MMA) return launch_mw(false, dev, c, x, W, y, M, N, K, N, reinterpret_cast<cudaStream_t>(stream));
     if (c.variant != DG_VAR_CC_WARP && c.variant != DG_VAR_CC_BULK) return DG_ERR_BAD_VARIANT;
     DenseArgs a{};
     a.W = static_cast<const uint8_t*>(W);
@@ -490,6 +496,8 @@ dg_status dg_gate_up_silu(const void* x, const void* W_gu, void* out, int M, int
     if (c.variant == DG_VAR_TC)
         return launch_tc(true, dev, c, x, W_gu, out, M, 2 * N_half, K, N_half, ws, ws_bytes,
                          reinterpret_cast<cudaStream_t>(stream));
+    if (c.variant == DG_VAR_MMA)
+        return launch_mw(true, dev, c, x, W_gu, out, M, 2 * N_half, K, N_half, reinterpret_cast<cudaStream_t>(stream));
     if (c.variant != DG_VAR_CC_WARP && c.variant != DG_VAR_CC_BULK) return DG_ERR_BAD_VARIANT;
     DenseArgs a{};
     a.W = static_cast<const uint8_t*>(W_gu);

@@ -33,6 +33,11 @@ struct DeviceInfo;
 dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W,
                     void* out, int M, int N, int K, int ld_out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+// Warp-level tensor-core family (dg_mma_dense.cu): bf16 linear (gate_up = false) or
+// interleaved gate/up rows, 1..16 token rows.
+dg_status launch_mw(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W, void* out,
+                    int M, int N, int K, int ld_out, cudaStream_t stream);
+
 // A8W8 block-scaled linear on the tcgen05 family (dg_tc_dense.cu): the fixed K-split
 // of a shape and the launcher; the activation quantisation alone (dg_a8.cu).
 constexpr int kA8MaxRows = 64;
@@ -104,8 +109,14 @@ constexpr size_t kMaxDynSmem = 200 * 1024;
 // Budget for staged activations of the dense CUDA-core family.
 constexpr size_t kXsBudget = 96 * 1024;
 
-// Smallest row bucket the bf16 linear and gate/up send to the tensor cores.
-constexpr int kTcMinRows = 3;
+// Row buckets of the bf16 linear and gate/up (measured on GB300, graph replay over
+// weights beyond L2): the CUDA cores below kMwMinRows*, the warp-level tensor cores
+// (mma.sync) up to kMwMaxRows*, the tcgen05 tiles above (always from the 16-row bucket).
+constexpr int kMwMinRowsLinear = 2;
+constexpr int kMwMinRowsGateUp = 3;
+constexpr int kMwMaxRowsLinear = 12;
+constexpr int kMwMaxRowsGateUp = 8;
+constexpr int kTcMinRows = 13;
 // Most token rows of one bf16 linear or gate/up call (the mid-M buckets 129..512 run
 // on the tensor cores in chunks of up to 256 tokens).
 constexpr int kMaxDenseRows = 512;

@@ -197,6 +197,15 @@ std::string check_choice(int op, const dg_choice& c)
             if (c.params[i] != 0) return "unused tensor-core parameter set";
         return "";
     }
+    if (c.variant == DG_VAR_MMA) {
+        if (op != DG_OP_GEMV_BF16 && op != DG_OP_GATE_UP_SILU) return "no warp-level tensor-core variant for this op";
+        const int ks = c.params[0], wpc = c.params[1], u = c.params[3];
+        if ((ks != 0 && ks != 1 && ks != 2 && ks != 4 && ks != 8) || (wpc != 0 && wpc != 4 && wpc != 8) ||
+            c.params[2] < 0 || (u != 0 && u != 2 && u != 4 && u != 8) || c.params[4] != 0 || c.params[5] != 0)
+            return "warp-level tensor-core parameters out of range";
+        if (ks > (wpc ? wpc : 8)) return "K-split warps must divide warps per CTA";
+        return "";
+    }
     if (c.variant == DG_VAR_CC_BULK) {
         if (op != DG_OP_GEMV_BF16 && op != DG_OP_GATE_UP_SILU && op != DG_OP_HEAD_FP8_ARGMAX)
             return "no bulk-staged variant for this op";
@@ -413,7 +422,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 9; }
+int dg_selection_space(void) { return 10; }
 
 const char* dg_build_id(void) { return build_id(); }
 

@@ -115,6 +115,13 @@ std::vector<dg_choice> candidates(int op, const dg_choice& def)
                 add(c);
             }
         }
+    } else if (def.variant == DG_VAR_MMA) {
+        for (int ks : {0, 1, 2, 4, 8})
+            for (int wpc : {0, 4, 8})
+                for (int u : {0, 2, 4, 8}) {
+                    if (wpc && ks > wpc) continue;
+                    add(mk(DG_VAR_MMA, ks, wpc, 0, u));
+                }
     } else if (op == DG_OP_MOE_W1 || op == DG_OP_MOE_W2) {
         const bool w1 = op == DG_OP_MOE_W1;
         for (int mt : {1, 2, 4})

@@ -86,7 +86,8 @@ typedef enum {
     DG_VAR_DEFAULT = 0,      /* let the library choose (same as choice == NULL) */
     DG_VAR_CC_WARP = 1,      /* CUDA cores, each warp streams R weight rows through registers */
     DG_VAR_CC_BULK = 2,      /* CUDA cores, bulk-async (TMA) copies stage weight rows in shared memory */
-    DG_VAR_TC = 3            /* tcgen05 tensor cores, TMA tiles, TMEM accumulators */
+    DG_VAR_TC = 3,           /* tcgen05 tensor cores, TMA tiles, TMEM accumulators */
+    DG_VAR_MMA = 4           /* warp-level tensor cores (mma.sync), weights streamed through registers */
 } dg_variant;
 
 /* params[] meaning by variant:
@@ -95,6 +96,10 @@ typedef enum {
  *                   sharing one row group's K segments (1, 2, 4, 8 dividing [1];
  *                   0 = 1) -- the segment partials are folded in the same order
  *   DG_VAR_CC_BULK: [0] 0, [1] pipeline stages (0 = as many as fit), [2] CTAs per SM (0 = 1)
+ *   DG_VAR_MMA:     bf16 linear and gate/up, 1..16 rows: [0] warps sharing one 16-row
+ *                   group's 512-element K segments (1, 2, 4, 8; 0 = derived), [1] warps per
+ *                   CTA (4 or 8; 0 = 8), [2] CTAs per SM cap (0 = occupancy limit), [3]
+ *                   32-element chunks per load round (2, 4, 8; 0 = 4)
  *   DG_VAR_TC:      [0] pipeline stages (0 = derived from the shape); bf16 linear and
  *                   gate/up: [1] K-split rule, 0 = sized by the shape and the row
  *                   count, 1 = by the shape alone (the batch-invariant mode's choice;

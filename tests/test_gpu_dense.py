@@ -30,7 +30,8 @@ def _lin_check(x, W, y, rows=None):
 CC = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0)
 BULK = dg.Choice.make(dg.DG_VAR_CC_BULK, 0, 0, 0)
 TC = dg.Choice.make(dg.DG_VAR_TC, 0)
-FAMILIES = {"cc": CC, "bulk": BULK, "tc": TC, "default": None}
+MMA = dg.Choice.make(dg.DG_VAR_MMA, 0, 0, 0, 0)
+FAMILIES = {"cc": CC, "bulk": BULK, "tc": TC, "mma": MMA, "default": None}
 SMALL = [(1, 2048, 1024), (3, 130, 1040), (5, 77, 520), (8, 300, 2056), (16, 96, 264), (37, 65, 136),
          (128, 64, 1024), (2, 1, 8), (16, 1000, 4096), (64, 300, 3000), (100, 257, 1096), (128, 640, 6144)]
 
@@ -289,3 +290,60 @@ def test_gate_up_mid_m(cuda_device, M):
     out = dg.dg_gate_up_silu(x, Wgu)
     torch.cuda.synchronize()
     _gate_up_check(x, Wgu, out)
+
+
+# ---------------------------------------------------------------- warp-level tensor cores (mma.sync)
+
+MMA_SMALL = [(3, 130, 1040), (5, 77, 520), (8, 300, 2056), (16, 96, 264), (1, 2048, 1024), (2, 1, 8),
+             (12, 1000, 4096), (9, 257, 1096), (16, 640, 6144), (4, 33, 4104), (15, 4099, 520)]
+
+
+@pytest.mark.parametrize("M,N,K", MMA_SMALL)
+def test_gemv_mma_small_exhaustive(cuda_device, M, N, K):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    y = dg.dg_gemv_bf16(x, W, choice=MMA)
+    torch.cuda.synchronize()
+    _lin_check(x, W, y)
+
+
+@pytest.mark.parametrize("N,K", SWEEP_NK)
+@pytest.mark.parametrize("M", [3, 4, 8, 12, 16])
+def test_gemv_mma_full_size_sampled(cuda_device, M, N, K):
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    y = dg.dg_gemv_bf16(x, W, choice=MMA)
+    torch.cuda.synchronize()
+    _lin_check(x, W, y, rows=sample_rows(N, 96, seed=N + K + 7 * M))
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 1000, 3080), (8, 300, 8200), (12, 77, 520), (16, 515, 1024), (5, 4096, 4096),
+                                   (9, 70, 2048)])
+def test_gemv_mma_variants_bitwise_identical(cuda_device, M, N, K):
+    """Every geometry of the warp-level tensor-core family (warps sharing a group's
+    segments, warps per CTA, CTA cap, chunks per load round) gives the same bits."""
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    ref = dg.dg_gemv_bf16(x, W, choice=MMA)
+    for ks, wpc, cap, u in itertools.product((1, 2, 4, 8), (4, 8), (0, 1), (2, 4, 8)):
+        if ks > wpc:
+            continue
+        y = dg.dg_gemv_bf16(x, W, choice=dg.Choice.make(dg.DG_VAR_MMA, ks, wpc, cap, u))
+        assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), (ks, wpc, cap, u)
+    for _ in range(3):
+        assert torch.equal(dg.dg_gemv_bf16(x, W, choice=MMA).view(torch.int16), ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,Nh,K", [(3, 96, 1040), (8, 300, 4096), (12, 12288, 4096), (16, 77, 2064)])
+def test_gate_up_mma(cuda_device, M, Nh, K):
+    x, Wgu = S.gate_up_inputs(M, Nh, K, device=cuda_device)
+    out = dg.dg_gate_up_silu(x, Wgu, choice=MMA)
+    torch.cuda.synchronize()
+    _gate_up_check(x, Wgu, out, cols=None if Nh <= 1000 else sample_rows(Nh, 96, seed=M))
+    for ks, wpc, u in ((1, 8, 4), (8, 8, 2), (2, 4, 8)):
+        o2 = dg.dg_gate_up_silu(x, Wgu, choice=dg.Choice.make(dg.DG_VAR_MMA, ks, wpc, 0, u))
+        assert torch.equal(o2.view(torch.int16), out.view(torch.int16)), (ks, wpc, u)
+
+
+def test_mma_refuses_more_than_16_rows(cuda_device):
+    x, W = S.linear_inputs(17, 64, 64, device=cuda_device)
+    with pytest.raises(dg.DGError) as e:
+        dg.dg_gemv_bf16(x, W, choice=MMA)
+    assert e.value.status == 3

@@ -26,8 +26,10 @@ CCW = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0)
 CCW_KS = dg.Choice.make(dg.DG_VAR_CC_WARP, 2, 8, 0, 4)      # four warps share a row group's segments
 BULK = dg.Choice.make(dg.DG_VAR_CC_BULK, 0, 0, 0)
 TC = dg.Choice.make(dg.DG_VAR_TC, 0)
+MMA = dg.Choice.make(dg.DG_VAR_MMA, 0, 0, 0, 0)
 LIN_CASES = [("cc", CCW, 1), ("cc_ksplit", CCW_KS, 2), ("bulk", BULK, 1), ("cc", CCW, 5),
-             ("tc", TC, 3), ("tc", TC, 16), ("tc", TC, 128), ("default", None, 8)]
+             ("tc", TC, 3), ("tc", TC, 16), ("tc", TC, 128), ("default", None, 8),
+             ("mma", MMA, 3), ("mma", MMA, 12), ("mma", MMA, 16)]
 LONG_K = [4096, 12288, 4096 + 16]
 
 

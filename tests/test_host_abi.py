@@ -91,8 +91,11 @@ def test_select_defaults_and_bucket_padding():
             w1 = op == dg.DG_OP_MOE_W1
             w2 = op == dg.DG_OP_MOE_W2
             # buckets: M=5 -> 6, M=7 -> 8
-            want = dg.DG_VAR_TC if ((dense_bf16 and M >= 3) or (head and M >= 2) or (w1 and M >= 7)
+            want = dg.DG_VAR_TC if ((dense_bf16 and M >= 13) or (head and M >= 2) or (w1 and M >= 7)
                                     or (w2 and M >= 4)) else dg.DG_VAR_CC_WARP
+            # the warp-level tensor cores take the linear at 2-12 rows and gate/up at 3-8
+            if dense_bf16 and ((2 <= M <= 12) if op == dg.DG_OP_GEMV_BF16 else (3 <= M <= 8)):
+                want = dg.DG_VAR_MMA
             assert c.variant == want and c.from_table == 0, (op, M, c)
     assert dg.dg_select(0, 129, 4096, 4096).variant == dg.DG_VAR_TC     # mid-M bucket 192
     with pytest.raises(dg.DGError):
@@ -215,7 +218,8 @@ def test_batch_invariant_numerics_takes_one_family_per_op():
         dg.dg_set_numerics(2)
     # the fastest mode mixes families across row buckets
     assert dg.dg_select(dg.DG_OP_GEMV_BF16, 1, 4096, 4096).variant == dg.DG_VAR_CC_WARP
-    assert dg.dg_select(dg.DG_OP_GEMV_BF16, 8, 4096, 4096).variant == dg.DG_VAR_TC
+    assert dg.dg_select(dg.DG_OP_GEMV_BF16, 8, 4096, 4096).variant == dg.DG_VAR_MMA
+    assert dg.dg_select(dg.DG_OP_GEMV_BF16, 16, 4096, 4096).variant == dg.DG_VAR_TC
     dg.dg_set_numerics(dg.DG_NUMERICS_BATCH_INVARIANT)
     try:
         assert dg.dg_numerics() == dg.DG_NUMERICS_BATCH_INVARIANT
