@@ -93,6 +93,23 @@ __device__ __forceinline__ void cluster_sync_all()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The same barrier in two halves: every thread arrives once, and waits (once) before
+// its next arrival or its first access to a peer's shared memory.  The arrival is
+// relaxed: the only data a peer reads before the next full barrier are the mbarriers,
+// published by fence.mbarrier_init.release.cluster before it.
+__device__ __forceinline__ void cluster_arrive()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Token stride (floats) of a parked partial tile: 144 = 128 rows + 16 puts consecutive
+// tokens 64 bytes apart modulo 128, so the fold's 16-byte reads of two tokens fall in
+// different bank halves (a stride of 128 rows sends every token to the same banks).
+constexpr int kPStride = 144;
+
 __device__ __forceinline__ uint32_t cluster_rank()
 {
     uint32_t r;
@@ -242,6 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool clustered = a.nsplit > 1;
+    // the parked partial tile takes the padded stride when the idle ring holds it
+    const int pstride = static_cast<size_t>(S) * kStage >= static_cast<size_t>(MP) * kPStride * 4 ? kPStride : kTileRows;
     const int tile = blockIdx.x / a.nsplit;
     const int split = clustered ? static_cast<int>(cluster_rank()) : 0;
     const int kb0 = static_cast<int>((static_cast<long long>(split) * a.nkb) / a.nsplit);
@@ -273,7 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
-    if (clustered) cluster_sync_all();     // every rank's barriers exist before any remote access
+    // Every rank's barriers exist before any remote access: arrive now, wait just before
+    // the first access to a peer (the producer streams meanwhile).
+    if (clustered) cluster_arrive();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t tmem = *tmem_holder;
     const uint32_t full0 = tc::su32(bars), empty0 = tc::su32(bars + S), accum = tc::su32(bars + 2 * S);
@@ -518,6 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (a.push) {
             // Push row `row` of this rank's partial tile (tokens 0..mq-1) into the
             // shared memory of the rank that folds it.
+            cluster_wait();
             if (good) {
                 int owner = 0;
                 while (owner + 1 < a.nsplit && row >= slice_lo(owner + 1, a.nsplit)) ++owner;
@@ -571,12 +593,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t v[16];
                 tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) P[(c * 16 + j) * kTileRows + row] = __uint_as_float(v[j]);
+                for (int j = 0; j < 16; ++j) P[(c * 16 + j) * pstride + row] = __uint_as_float(v[j]);
             }
         }
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     }
     if (clustered && !a.push) {
+        cluster_wait();                      // (the arrival at the start)
         cluster_sync_all();                  // every rank's partial tile is in place
         if (warp >= 2) {
             // This rank folds rows [lo, hi) (multiples of 4) for all tokens: P_0 + P_1 + ...
@@ -602,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         vv[u] = e < count;
                         tt[u] = vv[u] ? e / w4 : 0;
                         rr[u] = lo + 4 * (vv[u] ? e - tt[u] * w4 : 0);
-                        const uint32_t off = static_cast<uint32_t>((tt[u] * kTileRows + rr[u]) * 4);
+                        const uint32_t off = static_cast<uint32_t>((tt[u] * pstride + rr[u]) * 4);
                         acc[u] = vv[u] ? ld_dsmem_f32x4(peer[0] + off) : make_float4(0.f, 0.f, 0.f, 0.f);
                     }
                     // every rank's loads first (they overlap), then the adds in rank order
@@ -612,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int u = 0; u < 2; ++u)
                             pv[s2 - 1][u] = (s2 < a.nsplit && vv[u])
-                                ? ld_dsmem_f32x4(peer[s2] + static_cast<uint32_t>((tt[u] * kTileRows + rr[u]) * 4))
+                                ? ld_dsmem_f32x4(peer[s2] + static_cast<uint32_t>((tt[u] * pstride + rr[u]) * 4))
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int s2 = 1; s2 < kMaxCluster; ++s2) {
@@ -633,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cluster_sync_all();                  // no rank leaves while others still read its partials
     }
+    if (clustered && a.push && warp < 2) cluster_wait();   // (the arrival at the start)
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
     if (warp == 1) {
