@@ -186,6 +186,18 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device=dev)
     R = args.reps
 
+    table = None
+    if args.table:
+        # a shape table measured on this device and build (dg_sweep): every call
+        # below dispatches through it; the headline shapes are timed both ways
+        if args.sweep_table and rank == 0:
+            dg.dg_sweep(_table_shapes(dg), args.table, reps=args.sweep_reps, resume=True)
+        if world > 1:
+            dist.barrier()
+        with open(args.table) as f:
+            table = json.load(f)
+        dg.dg_table_load(args.table)
+
     cases = []        # (name, dict(meta), graph, weight_bytes_per_call)
     keep = []         # every tensor a captured graph reads or writes stays alive with it
     pattern = re.compile(args.cases) if args.cases else None
@@ -224,6 +236,12 @@ def run_gpu(args):
             ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K, device=dev)
             calls = [(lambda W=W, x=x, y=y, ws=ws: dg.dg_gemv_bf16(x, W, y, ws=ws, stream=stream)) for W in Ws]
             if wanted("gemv_bf16", {"M": M, "N": N, "K": K}):
+                if table is not None:
+                    # the same calls with the compiled defaults, captured before the
+                    # table is loaded again (dispatch happens when a call is captured)
+                    dg.dg_table_clear()
+                    add("gemv_bf16_defaults", {"M": M, "N": N, "K": K}, calls, wb)
+                    dg.dg_table_load(args.table)
                 add("gemv_bf16", {"M": M, "N": N, "K": K}, calls, wb)
                 sweep_cases.append(len(cases) - 1)
     def need(name, metas):
@@ -533,12 +551,48 @@ def run_gpu(args):
         "ops": ops,
         "timed_wall_s": round(wall, 3),
     }
+    if table is not None:
+        res["table"] = _table_report(table, args.table, dg, ops.pop("gemv_bf16_defaults", []), sweep, peak)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if world > 1:
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(res))
+
+
+def _table_shapes(dg):
+    """Every decode shape this benchmark times, as dg_sweep requests."""
+    sh = [(dg.DG_OP_GEMV_BF16, M, N, K, 0, 0) for (N, K) in SWEEP_NK for M in SWEEP_M]
+    sh.append((dg.DG_OP_GEMV_BF16, 1, 2048, 1024, 0, 0))
+    sh += [(dg.DG_OP_GATE_UP_SILU, M, 12288, 4096, 0, 0) for M in GATE_UP_M]
+    sh += [(dg.DG_OP_HEAD_FP8_ARGMAX, M, HEAD_N, HEAD_K, 0, 0) for M in HEAD_M]
+    sh += [(dg.DG_OP_MOE_W1, M, MOE_I, MOE_K, MOE_TOPK, MOE_E) for M in MOE_M]
+    sh += [(dg.DG_OP_MOE_W2, M, MOE_K, MOE_I, MOE_TOPK, MOE_E) for M in MOE_M]
+    return sh
+
+
+def _table_report(table, path, dg, defaults, sweep, peak):
+    """The headline sweep with the loaded table against the compiled defaults, both
+    timed in the same steps, plus the table's identity and the entries that differ."""
+    by = {(d["M"], d["N"], d["K"]): d for d in defaults}
+    rows, b_def, t_def = [], 0, 0.0
+    for s_ in sweep:
+        d = by.get((s_["M"], s_["N"], s_["K"]))
+        if d is None:
+            continue
+        b_def += d["weight_bytes"]
+        t_def += d["us"]
+        rows.append({"M": s_["M"], "N": s_["N"], "K": s_["K"], "us_table": s_["us"], "us_default": d["us"]})
+    changed = [e for e in table.get("entries", []) if e.get("pick") != e.get("default")]
+    v_def = b_def / (t_def * 1e-6) / 1e9 if t_def > 0 else None
+    return {"path": os.path.basename(path), "identity": table.get("identity"),
+            "entries": dg.dg_table_entries(), "entries_not_default": len(changed),
+            "defaults_value": round(v_def, 1) if v_def else None,
+            "defaults_frac": round(v_def / peak, 4) if v_def else None,
+            "changed": [{k: e.get(k) for k in ("op", "M", "N", "K", "pick", "pick_us", "default_us")}
+                        for e in changed],
+            "shapes": rows}
 
 
 def _e2e(torch, dg, S, dev, stream, args, l2):
@@ -738,6 +792,11 @@ def main():
     ap.add_argument("--cases", default="", help="profiling: regex over case ids such as 'moe_w2/M16' or "
                     "'head_fp8_argmax/M8/N248320/K4096' (only matching cases are built and timed)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--table", default="", help="dispatch through this shape table (dg_sweep JSON); the "
+                    "headline shapes are also timed with the compiled defaults")
+    ap.add_argument("--sweep-table", action="store_true", help="measure the table first (dg_sweep over "
+                    "every shape this benchmark times; resumes a partial table of this build)")
+    ap.add_argument("--sweep-reps", type=int, default=20)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
