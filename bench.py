@@ -221,6 +221,7 @@ def run_gpu(args):
 
     # --- the headline sweep
     sweep_cases = []
+    dcases = []       # shape-table arm: the sweep shapes' graphs with the compiled defaults
     only = None
     if args.only:
         only = tuple(int(v) for v in args.only.split(","))       # M,N,K
@@ -238,9 +239,11 @@ def run_gpu(args):
             if wanted("gemv_bf16", {"M": M, "N": N, "K": K}):
                 if table is not None:
                     # the same calls with the compiled defaults, captured before the
-                    # table is loaded again (dispatch happens when a call is captured)
+                    # table is loaded again (dispatch happens when a call is captured);
+                    # timed in steps of their own, in the same shape order
                     dg.dg_table_clear()
-                    add("gemv_bf16_defaults", {"M": M, "N": N, "K": K}, calls, wb)
+                    with torch.cuda.stream(stream):
+                        dcases.append(({"M": M, "N": N, "K": K}, _graph_case(torch, calls, R, stream), wb))
                     dg.dg_table_load(args.table)
                 add("gemv_bf16", {"M": M, "N": N, "K": K}, calls, wb)
                 sweep_cases.append(len(cases) - 1)
@@ -426,6 +429,24 @@ def run_gpu(args):
         dist.barrier()
     clk = clocks.stop()
 
+    # ---- shape-table arm: the same sweep with the compiled defaults, timed the same way
+    defaults = []
+    if dcases:
+        dev_ = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in dcases]
+        dts = [[] for _ in dcases]
+        with torch.cuda.stream(stream):
+            for step in range(args.warmup + args.steps):
+                for i, (_, g, _) in enumerate(dcases):
+                    dev_[i][0].record(stream)
+                    g.replay()
+                    dev_[i][1].record(stream)
+                stream.synchronize()
+                if step >= args.warmup:
+                    for i in range(len(dcases)):
+                        dts[i].append(dev_[i][0].elapsed_time(dev_[i][1]) * 1e3 / R)
+        defaults = [dict(**meta, us=round(statistics.median(t), 3), weight_bytes=int(wb))
+                    for (meta, _, wb), t in zip(dcases, dts)]
+
     # ---- cold single calls (outside the timed region): L2 flushed before each call
     cold = None
     if not args.no_cold and sweep_cases:
@@ -552,7 +573,7 @@ def run_gpu(args):
         "timed_wall_s": round(wall, 3),
     }
     if table is not None:
-        res["table"] = _table_report(table, args.table, dg, ops.pop("gemv_bf16_defaults", []), sweep, peak)
+        res["table"] = _table_report(table, args.table, dg, defaults, sweep, peak)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     if world > 1:
@@ -573,8 +594,9 @@ def _table_shapes(dg):
 
 
 def _table_report(table, path, dg, defaults, sweep, peak):
-    """The headline sweep with the loaded table against the compiled defaults, both
-    timed in the same steps, plus the table's identity and the entries that differ."""
+    """The headline sweep with the loaded table against the compiled defaults (timed
+    in steps of their own, the same way), plus the table's identity and the entries
+    that differ."""
     by = {(d["M"], d["N"], d["K"]): d for d in defaults}
     rows, b_def, t_def = [], 0, 0.0
     for s_ in sweep:

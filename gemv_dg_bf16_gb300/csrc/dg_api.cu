@@ -164,6 +164,13 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
             out->variant = DG_VAR_TC;
             break;
         }
+        if (M <= kMoeRangeMaxRowsW1) {         // one row range of every expert per CTA
+            out->params[0] = 4;
+            out->params[1] = 4;
+            out->params[4] = 2;
+            out->params[5] = kMoeOrderRange;
+            break;
+        }
         out->params[0] = 4;
         out->params[1] = 8;
         out->params[3] = M <= 1 ? 32 : (M <= 2 ? 64 : 0);
@@ -172,6 +179,13 @@ void default_choice(dg_op op, int M, int N, int K, dg_choice* out)
     case DG_OP_MOE_W2:
         if (M >= kTcMoeW2MinRows) {
             out->variant = DG_VAR_TC;
+            break;
+        }
+        if (M <= kMoeRangeMaxRowsW2) {
+            out->params[0] = 4;
+            out->params[1] = 8;
+            out->params[4] = 2;
+            out->params[5] = kMoeOrderRange;
             break;
         }
         out->params[0] = 4;
@@ -544,11 +558,52 @@ dg_status dg_head_fp8_argmax(const void* x, const void* Wq, const float* scale, 
                         reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Row-range order: grid = SMs x CTAs per SM (params[2], else the occupancy limit);
+// W2 cuts Nout into equal contiguous ranges (empty CTAs dropped), W1 the flattened
+// (expert, column pair) list.
+static dg_status launch_moe_range(bool w1, const DeviceInfo* dev, const dg_choice& c, MoeArgs a,
+                                  cudaStream_t stream)
+{
+    const int wpc = c.params[1] > 0 ? c.params[1] : 8;
+    const int mtmax = c.params[4] > 0 ? c.params[4] : 2;
+    if ((c.params[0] != 0 && c.params[0] != 4) || (wpc != 4 && wpc != 8) || c.params[2] < 0 || c.params[2] > 4 ||
+        c.params[3] != 0)
+        return DG_ERR_BAD_VARIANT;
+    const void* fn = moe_range_kernel_fn(w1, mtmax);
+    if (!fn) return DG_ERR_BAD_VARIANT;
+    const int threads = wpc * 32;
+    const int rows = w1 ? a.I : a.Nout;
+    // shared memory at the widest range any grid of >= one CTA per SM gives
+    const int rpc_max = w1 ? 0 : (rows + dev->sm_count - 1) / dev->sm_count;
+    size_t smem = moe_range_smem(w1, a.M, a.topk, a.K, rpc_max);
+    if (smem > kMaxDynSmem) return DG_ERR_UNSUPPORTED_SHAPE;
+    int occ = occupancy(fn, threads, smem);
+    if (occ < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+    if (c.params[2] > 0 && occ > c.params[2]) occ = c.params[2];
+    long long grid = static_cast<long long>(dev->sm_count) * occ;
+    a.tile = 0;
+    if (!w1) {
+        if (grid > rows) grid = rows;
+        const long long rpc = (rows + grid - 1) / grid;
+        grid = (rows + rpc - 1) / rpc;                      // every CTA has rows
+        a.tile = static_cast<int>(rpc);
+        smem = moe_range_smem(false, a.M, a.topk, a.K, a.tile);
+    }
+    void* args[] = {&a};
+    if (launch_kernel(fn, static_cast<unsigned>(grid), threads, smem, stream, args) != cudaSuccess) {
+        cudaGetLastError();
+        return DG_ERR_CUDA;
+    }
+    return DG_OK;
+}
+
 static dg_status launch_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, MoeArgs a,
                             cudaStream_t stream)
 {
     if (c.variant == DG_VAR_TC) return launch_tc_moe(w1, dev, c, a, stream);
     if (c.variant != DG_VAR_CC_WARP) return DG_ERR_BAD_VARIANT;
+    if (c.params[5] == kMoeOrderRange) return launch_moe_range(w1, dev, c, a, stream);
+    if (c.params[5] != 0 && c.params[5] != kMoeOrderUnits) return DG_ERR_BAD_VARIANT;
     const int wpc = c.params[1] > 0 ? c.params[1] : 8;
     if (c.params[0] != 0 && c.params[0] != 4) return DG_ERR_BAD_VARIANT;
     if (wpc < 1 || wpc > 8 || c.params[2] < 0 || c.params[3] < 0) return DG_ERR_BAD_VARIANT;

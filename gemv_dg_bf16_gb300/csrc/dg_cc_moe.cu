@@ -17,6 +17,7 @@
 #include "dg_cc_dense.cuh"
 #include "dg_internal.h"
 #include "dg_moe.cuh"
+#include "dg_tc_common.cuh"
 
 namespace dg {
 
@@ -207,7 +208,298 @@ __global__ void __launch_bounds__(256, MTMAX <= 2 ? 3 : 2) moe_kernel(MoeArgs a)
     }
 }
 
+// ------------------------------------------------------------------ row ranges
+// The same outputs in the same arithmetic, cut the other way: CTA b owns one
+// contiguous range of rows of EVERY active expert, so no output is shared between
+// CTAs.  W2: output rows n in [lo, hi); each (slot, n) term stays in shared memory and
+// the CTA folds y[t, n] over the valid slots in slot order at the end -- no ticket,
+// no fence, no pass through the workspace.  W1 has no combine: the CTA takes a
+// contiguous share of the flattened (active expert, column pair) list, so the share
+// is even to one column pair whatever the expert count.  The activation rows (W2:
+// all M x topk rows of a; W1: the M rows of x) do not depend on the routing: one bulk
+// copy brings them into shared memory while the routing is built.  A warp loads two K segments of its rows before folding the first, which
+// halves the dependent memory round trips of an item.
+
+// Canonical-order partial of segment s for R rows x MT pairs whose activation rows sit
+// anywhere in shared memory (xr[t] = pair t's row): fold_segment's arithmetic with the
+// activation rows gathered instead of strided.
+template <int MT, int R>
+__device__ __forceinline__ void fold_gathered(const uint4 (&w)[kSeg / (32 * WTraits<WT_E4M3>::VE)][R], int K, int s,
+                                              const uint4* const (&xr)[MT], int lane, float& total)
+{
+    constexpr int VE = WTraits<WT_E4M3>::VE;
+    constexpr int VPS = kSeg / (32 * VE);
+    constexpr int MTP = cpow2(MT);
+    constexpr int Q = R * MTP;
+    float p[Q];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) p[q] = 0.0f;
+#pragma unroll
+    for (int v = 0; v < VPS; ++v) {
+        const int k = s * kSeg + v * (32 * VE) + lane * VE;
+        if (k >= K) continue;
+        // 16 e4m3 weights = two halves of 8, each against one bf16 vector of x
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint4 xv[MT];
+#pragma unroll
+            for (int t = 0; t < MT; ++t) xv[t] = xr[t][k / 8 + h];
+#pragma unroll
+            for (int ww = 0; ww < 2; ++ww) {
+#pragma unroll
+                for (int pp = 0; pp < 2; ++pp) {
+                    float x0[MT], x1[MT];
+#pragma unroll
+                    for (int t = 0; t < MT; ++t) {
+                        const uint32_t xw = (&xv[t].x)[2 * ww + pp];
+                        x0[t] = bf16_lo(xw);
+                        x1[t] = bf16_hi(xw);
+                    }
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const uint32_t wword = (&w[v][r].x)[2 * h + ww];
+                        const float2 wf = e4m3x2_to_f32(pp ? (wword >> 16) : wword);
+#pragma unroll
+                        for (int t = 0; t < MT; ++t) {
+                            float acc = p[r * MTP + t];
+                            acc = __fmaf_rn(x0[t], wf.x, acc);
+                            acc = __fmaf_rn(x1[t], wf.y, acc);
+                            p[r * MTP + t] = acc;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    reduce_scatter<Q>(p, lane);
+    total = (s == 0) ? p[0] : total + p[0];
+}
+
+// Row total over all segments: for one pair two segments' loads in flight at a time,
+// for more pairs one (the accumulators need the registers).
+template <int MT, int R>
+__device__ __forceinline__ float gathered_total(const uint8_t* const (&wrow)[R], const bool (&rok)[R], int K,
+                                                const uint4* const (&xr)[MT], int lane)
+{
+    constexpr int VPS = kSeg / (32 * WTraits<WT_E4M3>::VE);
+    const int nseg = (K + kSeg - 1) / kSeg;
+    float total = 0.0f;
+    if constexpr (MT > 1) {
+        for (int s = 0; s < nseg; ++s) {
+            uint4 w0[VPS][R];
+            load_segment<WT_E4M3, R>(w0, wrow, rok, K, s, lane);
+            fold_gathered<MT, R>(w0, K, s, xr, lane, total);
+        }
+    } else {
+        for (int s = 0; s < nseg; s += 2) {
+            uint4 w0[VPS][R], w1[VPS][R];
+            load_segment<WT_E4M3, R>(w0, wrow, rok, K, s, lane);
+            if (s + 1 < nseg) load_segment<WT_E4M3, R>(w1, wrow, rok, K, s + 1, lane);
+            fold_gathered<MT, R>(w0, K, s, xr, lane, total);
+            if (s + 1 < nseg) fold_gathered<MT, R>(w1, K, s + 1, xr, lane, total);
+        }
+    }
+    return total;
+}
+
+// Shared-memory layout of the row-range kernel, the same on host and device:
+// activation rows (W2: the M x topk rows of a; W1: the M rows of x), then W2's terms
+// [M x topk slots][rows per CTA].
+__host__ __device__ inline size_t range_xs_bytes(bool w1, int M, int topk, int K)
+{
+    return static_cast<size_t>(w1 ? M : M * topk) * K * 2;
+}
+
+__host__ __device__ inline size_t range_smem_bytes(bool w1, int M, int topk, int K, int rpc)
+{
+    return range_xs_bytes(w1, M, topk, K) + (w1 ? 0 : static_cast<size_t>(M) * topk * rpc * 4);
+}
+
+// One item: R rows of expert u for pairs [p0, p0 + MT), the emitted outputs as in
+// w1_chunk / w2_chunk (W2's terms into shared memory instead of the workspace).
+template <bool W1, int MT>
+__device__ void range_item(const MoeArgs& a, const Route& R, int e, int r0, int p0, const uint4* xs,
+                           float* terms, int lo, int hi, int rpc)
+{
+    constexpr int RH = kMoeR / 2;
+    constexpr int MTP = cpow2(MT);
+    constexpr int Q = kMoeR * MTP;
+    constexpr int SH = 5 - clog2(Q);
+    const int lane = threadIdx.x & 31;
+    const int idx = lane >> SH, my_r = idx / MTP, my_t = idx % MTP;
+    const int kv = a.K / 8;
+    const uint4* xr[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t)
+        xr[t] = xs + static_cast<size_t>(W1 ? R.ptok[p0 + t] : R.ptok[p0 + t] * a.topk + R.pslot[p0 + t]) * kv;
+    const uint8_t* wrow[kMoeR];
+    bool rok[kMoeR];
+    if constexpr (W1) {
+        // r0 = first column j of the item; rows j, j+1 (gate) and I+j, I+j+1 (up)
+        const uint8_t* We = a.W + static_cast<size_t>(e) * 2 * a.I * a.K;
+#pragma unroll
+        for (int r = 0; r < kMoeR; ++r) {
+            const int j = r0 + (r % RH);
+            rok[r] = j < a.I;
+            wrow[r] = We + static_cast<size_t>((r < RH ? 0 : a.I) + (rok[r] ? j : r0)) * a.K;
+        }
+        const float total = gathered_total<MT, kMoeR>(wrow, rok, a.K, xr, lane);
+        const float up = __shfl_sync(kFull, total, (lane + ((RH * MTP) << SH)) & 31);
+        const int j = r0 + my_r;
+        const bool writer = (lane & ((1 << SH) - 1)) == 0 && my_t < MT && my_r < RH;
+        if (writer && j < a.I) {
+            const float g = total * a.s[static_cast<size_t>(e) * 2 * a.I + j];
+            const float u = up * a.s[static_cast<size_t>(e) * 2 * a.I + a.I + j];
+            const float silu = g / (1.0f + expf(-g));
+            const int t = R.ptok[p0 + my_t], k = R.pslot[p0 + my_t];
+            a.out[(static_cast<size_t>(t) * a.topk + k) * a.I + j] = f32_to_bf16_bits(silu * u);
+        }
+    } else {
+        // r0 = first output row n of the item (rows n < hi of this CTA's range)
+        const uint8_t* We = a.W + static_cast<size_t>(e) * a.Nout * a.K;
+#pragma unroll
+        for (int r = 0; r < kMoeR; ++r) {
+            rok[r] = r0 + r < hi;
+            wrow[r] = We + static_cast<size_t>(rok[r] ? r0 + r : lo) * a.K;
+        }
+        const float total = gathered_total<MT, kMoeR>(wrow, rok, a.K, xr, lane);
+        const int n = r0 + my_r;
+        const bool writer = (lane & ((1 << SH) - 1)) == 0 && my_t < MT;
+        if (writer && n < hi) {
+            const int t = R.ptok[p0 + my_t], k = R.pslot[p0 + my_t];
+            const float h = total * a.s[static_cast<size_t>(e) * a.Nout + n];
+            terms[(t * a.topk + k) * rpc + (n - lo)] = h * a.gw[t * a.topk + k];
+        }
+    }
+}
+
+template <bool W1, int MTMAX>
+__device__ void range_items(int c, const MoeArgs& a, const Route& R, int e, int r0, int p0, const uint4* xs,
+                            float* terms, int lo, int hi, int rpc)
+{
+#define DG_MOE_CASE(MT)                                                                    \
+    case MT:                                                                               \
+        if constexpr (MT <= MTMAX) range_item<W1, MT>(a, R, e, r0, p0, xs, terms, lo, hi, rpc); \
+        break;
+    switch (c) {
+        DG_MOE_CASE(1) DG_MOE_CASE(2) DG_MOE_CASE(3) DG_MOE_CASE(4)
+        DG_MOE_CASE(5) DG_MOE_CASE(6) DG_MOE_CASE(7) DG_MOE_CASE(8)
+    default: break;
+    }
+#undef DG_MOE_CASE
+}
+
+template <bool W1, int MTMAX>
+__global__ void __launch_bounds__(256, 2) moe_range_kernel(MoeArgs a)
+{
+    __shared__ Route R;
+    __shared__ __align__(8) uint64_t xbar;        // the activation copy's completion
+    __shared__ int abort_s;
+    extern __shared__ __align__(128) uint4 xs[];
+    pdl_launch_dependents();
+    pdl_wait();                                    // routing and activations come from earlier kernels
+    const int kv = a.K / 8;
+    const int P_all = a.M * a.topk;
+    // The slot ids first (their latency overlaps the rest of the prologue), then one
+    // bulk copy of every activation row the call can use, in row order (W2: the
+    // M x topk rows of a, row t * topk + k; W1: the M rows of x), then the routing.
+    const int e_lane = P_all <= 32 ? route_warp_load(a.ids, P_all) : -1;
+    if (threadIdx.x == 0) {
+        abort_s = 0;
+        const uint32_t bar = tc::su32(&xbar);
+        tc::bar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const uint32_t bytes = static_cast<uint32_t>(range_xs_bytes(W1, a.M, a.topk, a.K));
+        tc::bar_expect_tx(bar, bytes);
+        asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                         tc::su32(xs)),
+                     "l"(a.x), "r"(bytes), "r"(bar)
+                     : "memory");
+    }
+    if (P_all <= 32) route_warp_build(R, e_lane, a.M, a.topk, a.E, a.ws);
+    else route_scan(R, a.ids, a.M, a.topk, a.E, a.ws);
+
+    const int warp = threadIdx.x >> 5, wpc = blockDim.x >> 5;
+    constexpr int RH = kMoeR / 2;
+    // This CTA's share.  W2: rows [lo, hi) of every expert (rpc = a.tile rows per CTA,
+    // the grid = ceil(Nout / rpc)).  W1: items [it_lo, it_hi) of the list (active
+    // expert u, column pair jg), u-major.
+    const int rpc = W1 ? 0 : a.tile;
+    const int lo = W1 ? 0 : blockIdx.x * rpc;
+    const int hi = W1 ? 0 : min(a.Nout, lo + rpc);
+    const int ipe = W1 ? (a.I + RH - 1) / RH : (rpc + kMoeR - 1) / kMoeR;      // items per expert
+    int it_lo, it_hi;                              // at most 1024 experts x 4096 items
+    if constexpr (W1) {
+        const long long n = static_cast<long long>(R.U) * ipe;
+        it_lo = static_cast<int>(n * blockIdx.x / gridDim.x);
+        it_hi = static_cast<int>(n * (blockIdx.x + 1) / gridDim.x);
+    } else {
+        it_lo = 0;
+        it_hi = lo < hi ? R.U * ipe : 0;
+    }
+    if constexpr (W1) {
+        // invalid slots get a = 0: this CTA clears its share of the columns
+        const int j_lo = static_cast<int>(static_cast<long long>(a.I) * blockIdx.x / gridDim.x);
+        const int j_hi = static_cast<int>(static_cast<long long>(a.I) * (blockIdx.x + 1) / gridDim.x);
+        for (int i = 0; i < a.M * a.topk; ++i)
+            if (!R.valid[i])
+                for (int j = j_lo + threadIdx.x; j < j_hi; j += blockDim.x) a.out[static_cast<size_t>(i) * a.I + j] = 0;
+    }
+    if (threadIdx.x == 0) tc::bar_wait(tc::su32(&xbar), 0, &abort_s);
+    __syncthreads();
+    if (abort_s) {                                 // the activation copy never landed
+        if (threadIdx.x == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
+        return;
+    }
+    float* terms = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xs) + range_xs_bytes(W1, a.M, a.topk, a.K));
+
+    for (int it = it_lo + warp; it < it_hi; it += wpc) {
+        const int u = it / ipe, g = it - u * ipe;
+        const int e = R.experts[u];
+        const int r0 = W1 ? g * RH : lo + g * kMoeR;
+        if (!W1 && r0 >= hi) continue;                 // the last CTA's short range
+        const int pb = R.offs[u], pe = R.offs[u + 1];
+        for (int p0 = pb; p0 < pe; p0 += MTMAX)
+            range_items<W1, MTMAX>(min(MTMAX, pe - p0), a, R, e, r0, p0, xs, terms, lo, hi, rpc);
+    }
+    if constexpr (!W1) {
+        __syncthreads();
+        // y[t, n] = the valid slots' terms folded in slot order (0 for a token with none)
+        const int w = hi - lo;
+        for (int i = threadIdx.x; i < a.M * w; i += blockDim.x) {
+            const int t = i / w, n = lo + (i - t * w);
+            float y = 0.0f;
+            bool first = true;
+            for (int k = 0; k < a.topk; ++k) {
+                if (!R.valid[t * a.topk + k]) continue;
+                const float v = terms[(t * a.topk + k) * rpc + (n - lo)];
+                y = first ? v : y + v;
+                first = false;
+            }
+            a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
+        }
+    }
+}
+
 }  // namespace
+
+size_t moe_range_smem(bool w1, int M, int topk, int K, int rpc) { return range_smem_bytes(w1, M, topk, K, rpc); }
+
+const void* moe_range_kernel_fn(bool w1, int mtmax)
+{
+    switch (mtmax) {
+    case 1: return w1 ? reinterpret_cast<const void*>(&moe_range_kernel<true, 1>)
+                      : reinterpret_cast<const void*>(&moe_range_kernel<false, 1>);
+    case 2: return w1 ? reinterpret_cast<const void*>(&moe_range_kernel<true, 2>)
+                      : reinterpret_cast<const void*>(&moe_range_kernel<false, 2>);
+    case 4: return w1 ? reinterpret_cast<const void*>(&moe_range_kernel<true, 4>)
+                      : reinterpret_cast<const void*>(&moe_range_kernel<false, 4>);
+    case 8: return w1 ? reinterpret_cast<const void*>(&moe_range_kernel<true, 8>)
+                      : reinterpret_cast<const void*>(&moe_range_kernel<false, 8>);
+    default: return nullptr;
+    }
+}
 
 const void* moe_w1_kernel(int mtmax)
 {

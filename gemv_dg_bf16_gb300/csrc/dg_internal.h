@@ -22,6 +22,10 @@ const void* bulk_kernel_head(int mt);
 // MoE kernels by the most (token, slot) pairs one pass handles (1, 2, 4 or 8).
 const void* moe_w1_kernel(int mtmax);
 const void* moe_w2_kernel(int mtmax);
+// The row-range MoE kernel (one contiguous row range of every active expert per CTA)
+// and its dynamic shared memory for rpc output rows per CTA (W2; 0 for W1).
+const void* moe_range_kernel_fn(bool w1, int mtmax);
+size_t moe_range_smem(bool w1, int M, int topk, int K, int rpc);
 
 // tcgen05 family (dg_tc_dense.cu): padded token count, fixed K-split of a shape,
 // workspace bytes, and the launcher (bf16 linear or interleaved gate/up rows).
@@ -59,11 +63,19 @@ dg_status launch_tc_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, cons
 // Smallest row bucket the fp8 head sends to the tensor cores, and the largest K
 // whose split activations fit in shared memory.
 constexpr int kTcHeadMinRows = 2;
-// Smallest row buckets the MoE calls send to the tensor cores (measured on GB300:
-// W2's grid-barrier combine makes its tensor-core kernel the faster one from 4
-// token rows, W1's from 8).
+// Smallest row buckets the MoE calls send to the tensor cores, and the largest that
+// take the CUDA-core row-range order (measured on GB300 with graphs of 16 calls over
+// 8 routings: the row-range W2 beats the tensor cores up to 4 token rows, 35.3 vs
+// 38.0 us at 4; the tensor cores win from 6 rows up, the (expert, N-tile) order
+// takes W1 at 3-6 rows).
 constexpr int kTcMoeW1MinRows = 8;
-constexpr int kTcMoeW2MinRows = 4;
+constexpr int kTcMoeW2MinRows = 5;
+constexpr int kMoeRangeMaxRowsW1 = 2;
+constexpr int kMoeRangeMaxRowsW2 = 4;
+// Work order of the CUDA-core MoE kernels (choice params[5]): (expert, N-tile) units
+// walked by persistent CTAs, or one contiguous row range of every expert per CTA.
+constexpr int kMoeOrderUnits = 1;
+constexpr int kMoeOrderRange = 2;
 constexpr int kTcHeadMaxK = 8192;
 
 struct DeviceInfo {

@@ -49,11 +49,78 @@ struct Route {
     int cnt[kMoeMaxE];               // per expert: pair count, then pair offset
 };
 
+// Up to 32 slots: warp 0 builds every table, one slot per lane (one global load, no
+// shared-memory passes over the experts, one barrier).  Lane i holds slot i = (t, k);
+// its pair position is the number of valid slots with a smaller expert id plus the
+// earlier valid slots of the same expert (ascending expert, then token, then slot);
+// its expert's index is the number of distinct smaller experts.  The load and the
+// build are separate steps so that a kernel can issue other copies in between.
+__device__ __forceinline__ int route_warp_load(const int32_t* __restrict__ ids, int P_all)
+{
+    return (threadIdx.x < 32 && static_cast<int>(threadIdx.x) < P_all) ? ids[threadIdx.x] : -1;
+}
+
+__device__ inline void route_warp_build(Route& R, int e, int M, int topk, int E, uint8_t* ws)
+{
+    __shared__ int se[32];
+    const int P_all = M * topk;
+    if (threadIdx.x < 32) {
+        const int i = threadIdx.x;
+        const bool in = i < P_all;
+        se[i] = e;
+        __syncwarp();
+        const int t = in ? i / topk : 0, k = in ? i - t * topk : 0;
+        bool ok = in && e >= 0 && e < E;
+        for (int j = 0; j < k; ++j)
+            if (se[t * topk + j] == e) ok = false;
+        const unsigned vmask = __ballot_sync(kFull, ok);
+        int smaller = 0, same_before = 0;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) {
+            const int ej = se[j];
+            const bool vj = (vmask >> j) & 1u;
+            smaller += (vj && ej < e) ? 1 : 0;
+            same_before += (vj && ej == e && j < i) ? 1 : 0;
+        }
+        const bool first = ok && same_before == 0;
+        const unsigned fmask = __ballot_sync(kFull, first);
+        int u = 0;
+#pragma unroll 8
+        for (int j = 0; j < 32; ++j) u += (((fmask >> j) & 1u) && se[j] < e) ? 1 : 0;
+        if (in) R.valid[i] = ok ? 1 : 0;
+        if (in && !ok && blockIdx.x == 0) set_status(ws, DG_DEVERR_BAD_TOPK_ID);
+        if (ok) {
+            const int pos = smaller + same_before;
+            R.ptok[pos] = static_cast<int8_t>(t);
+            R.pslot[pos] = static_cast<int8_t>(k);
+            if (first) {
+                R.experts[u] = static_cast<int16_t>(e);
+                R.offs[u] = static_cast<int16_t>(smaller);
+            }
+        }
+        const int U = __popc(fmask), P = __popc(vmask);
+        if (i == 0) {
+            R.U = U;
+            R.P = P;
+            R.offs[U] = static_cast<int16_t>(P);
+        }
+        if (i < M) {
+            const unsigned tok = ((1u << topk) - 1u) << (i * topk);
+            R.nvalid[i] = __popc(vmask & tok);
+        }
+    }
+    __syncthreads();
+}
+
 // Every CTA computes the same routing tables (deterministic, no atomics on order).
 // topk_ids is read from global memory once, into shared memory.
 __device__ inline void route_scan(Route& R, const int32_t* __restrict__ ids, int M, int topk, int E,
                            uint8_t* ws)
 {
+    if (M * topk <= 32) {
+        route_warp_build(R, route_warp_load(ids, M * topk), M, topk, E, ws);
+        return;
+    }
     __shared__ int sid[kMoeMaxPairs];
     const int P_all = M * topk;
     for (int i = threadIdx.x; i < P_all; i += blockDim.x) sid[i] = ids[i];

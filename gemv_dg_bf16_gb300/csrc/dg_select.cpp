@@ -220,6 +220,10 @@ std::string check_choice(int op, const dg_choice& c)
         if (R != 0 && R != 4) return "MoE rows per warp must be 4";
         const int mt = c.params[4];
         if (mt != 0 && mt != 1 && mt != 2 && mt != 4 && mt != 8) return "MoE pairs per pass must be 1, 2, 4 or 8";
+        if (c.params[5] != 0 && c.params[5] != kMoeOrderUnits && c.params[5] != kMoeOrderRange)
+            return "MoE work order must be 0, 1 or 2";
+        if (c.params[5] == kMoeOrderRange && ((wpc != 4 && wpc != 8) || c.params[2] > 4 || c.params[3] != 0))
+            return "MoE row-range parameters out of range";
     } else if (R != 1 && R != 2 && R != 4 && R != 8) {
         return "rows per warp must be 1, 2, 4 or 8";
     }
@@ -422,7 +426,7 @@ using namespace dg;
 
 extern "C" {
 
-int dg_selection_space(void) { return 10; }
+int dg_selection_space(void) { return 11; }
 
 const char* dg_build_id(void) { return build_id(); }
 

@@ -131,6 +131,22 @@ std::vector<dg_choice> candidates(int op, const dg_choice& def)
                     c.params[4] = mt;
                     add(c);
                 }
+        // one row range of every expert per CTA: warps and CTAs per SM, pairs per pass
+        for (int mt : {1, 2, 4})
+            for (int wpc : {4, 8})
+                for (int cps : {0, 1, 3}) {
+                    dg_choice c = mk(DG_VAR_CC_WARP, 4, wpc, cps, 0);
+                    c.params[4] = mt;
+                    c.params[5] = kMoeOrderRange;
+                    add(c);
+                }
+        // and the other order, whichever is the default
+        for (int wpc : {4, 8}) {
+            dg_choice c = mk(DG_VAR_CC_WARP, 4, wpc, 0, 0);
+            c.params[4] = 2;
+            c.params[5] = def.params[5] == kMoeOrderRange ? kMoeOrderUnits : kMoeOrderRange;
+            add(c);
+        }
     } else {
         for (int R : {1, 2, 4, 8})
             for (int wpc : {4, 8})

@@ -106,9 +106,16 @@ typedef enum {
  *                   the two agree up to 128 rows); A8W8: [1] 1 = quantise the activations
  *                   in a launch of its own into the workspace and stream the codes by TMA
  *                   (0 = the quantisation fused into the tensor-core kernel; same bits)
- * For the MoE ops, params[3] is the N-tile width in rows (0 = derived) and
- * params[4] the most (token, slot) pairs of one expert per pass over its rows
- * (1, 2, 4 or 8; 0 = 2). */
+ * For the MoE ops (DG_VAR_CC_WARP), params[5] is the work order: 0 or 1 = persistent
+ * CTAs walk (active expert, N-tile) units, params[3] the N-tile width in rows (0 =
+ * derived); 2 = each CTA owns one contiguous row range of every active expert (W2:
+ * output rows, folded over the slots inside the CTA; W1: an even share of the
+ * (expert, column pair) list), params[1] warps per CTA 4 or 8, params[2] CTAs per SM
+ * (0 = the occupancy limit, at most 4), params[3] 0; W2 in this order keeps all M *
+ * topk activation rows in shared memory (M * topk * I * 2 bytes, at most 200 KiB, else
+ * DG_ERR_UNSUPPORTED_SHAPE).  params[4] is, in both orders, the most
+ * (token, slot) pairs of one expert per pass over its rows (1, 2, 4 or 8; 0 = 2).
+ * Both orders give the same bits. */
 typedef struct {
     int32_t variant;
     int32_t params[6];

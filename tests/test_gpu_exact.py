@@ -112,13 +112,14 @@ def _dec(codes_u8):
     return torch.from_numpy(np.ascontiguousarray(codes_u8)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
 
 
-@pytest.mark.parametrize("family", ["default", "cc", "tc"])
+@pytest.mark.parametrize("family", ["default", "cc", "tc", "range"])
 @pytest.mark.parametrize("M", [1, 2, 4, 8])
 def test_moe_end_to_end_against_oracle(cuda_device, moe_w, M, family):
     """y = W2(silu(W1 x)) through both kernels, against the fp64 chain on the oracle's
     own activations: |y - y_ref| <= W2's bound on the GPU's a + sum_k |gw| s2 |W2| err_a,
     err_a being W1's bound for each element of a."""
-    choice = {"default": None, "cc": dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, 2), "tc": TC}[family]
+    choice = {"default": None, "cc": dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, 2), "tc": TC,
+              "range": dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, 2, 2)}[family]
     W1q, s1, W2q, s2 = moe_w
     x, ids, gw = S.moe_inputs(M, KH, TOPK, E, rep=5, device=cuda_device)
     a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=choice)

@@ -15,7 +15,10 @@ E, I, K, TOPK = 128, 1536, 4096, 6
 MOE_M = [1, 2, 4, 8, 16]
 CC = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, 2)
 TC = dg.Choice.make(dg.DG_VAR_TC, 0)
-FAMILIES = {"cc": CC, "tc": TC, "default": None}
+# the CUDA-core kernels in row-range order (one contiguous row range of every expert per CTA)
+RANGE = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, 0, 2)
+FAMILIES = {"cc": CC, "tc": TC, "range": RANGE, "default": None}
+RANGE_W2_MAX_M = 10        # every pair's activation row of the call fits in shared memory
 
 
 @pytest.fixture(scope="module")
@@ -43,7 +46,7 @@ def _w2_ref(a, ids, gw, W2q, s2):
     return O.moe_w2(bits16(a), ids_c, gw.cpu().numpy(), w2, sc2)
 
 
-@pytest.mark.parametrize("family", ["cc", "tc"])
+@pytest.mark.parametrize("family", ["cc", "tc", "range"])
 @pytest.mark.parametrize("M", MOE_M)
 def test_moe_w1_full_size(cuda_device, moe_w, M, family):
     W1q, s1, W2q, s2 = moe_w
@@ -57,9 +60,11 @@ def test_moe_w1_full_size(cuda_device, moe_w, M, family):
     assert dg.dg_device_status(ws) == 0
 
 
-@pytest.mark.parametrize("family", ["cc", "tc"])
+@pytest.mark.parametrize("family", ["cc", "tc", "range"])
 @pytest.mark.parametrize("M", MOE_M)
 def test_moe_w2_full_size_on_gpu_activations(cuda_device, moe_w, M, family):
+    if family == "range" and M > RANGE_W2_MAX_M:
+        pytest.skip("the row-range W2 keeps every pair's row in shared memory")
     W1q, s1, W2q, s2 = moe_w
     c = FAMILIES[family]
     x, ids, gw = S.moe_inputs(M, K, TOPK, E, device=cuda_device)
@@ -105,7 +110,61 @@ def test_moe_tiles_and_warps_bitwise_identical(cuda_device, moe_w, M):
                 assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (wpc, tile, mt)
 
 
-@pytest.mark.parametrize("family", ["cc", "tc"])
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8])
+def test_moe_range_order_bitwise_identical_to_units(cuda_device, moe_w, M):
+    """The row-range order computes every output with the same canonical chain as the
+    (expert, N-tile) order: the same bits for every geometry."""
+    W1q, s1, W2q, s2 = moe_w
+    x, ids, gw = S.moe_inputs(M, K, TOPK, E, rep=11, device=cuda_device)
+    a_ref = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=CC)
+    y_ref = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2, choice=CC)
+    for wpc in (4, 8):
+        for cps in (0, 1, 2, 3):
+            for mt in (0, 1, 2, 4, 8):
+                c = dg.Choice.make(dg.DG_VAR_CC_WARP, 4, wpc, cps, 0, mt, 2)
+                a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=c)
+                assert torch.equal(a.view(torch.int16), a_ref.view(torch.int16)), (wpc, cps, mt)
+                y = dg.dg_moe_w2(a_ref, ids, gw, W2q, s2, choice=c)
+                assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16)), (wpc, cps, mt)
+
+
+@pytest.mark.parametrize("M,E_,I_,K_,Nout,topk", [(1, 8, 80, 272, 100, 3), (3, 8, 80, 272, 100, 3),
+                                                  (2, 16, 208, 64, 1000, 5), (7, 4, 16, 16, 9, 2),
+                                                  (10, 128, 1536, 4096, 4096, 6)])
+def test_moe_range_order_ragged_shapes(cuda_device, M, E_, I_, K_, Nout, topk):
+    """Ranges of one row, CTAs with no work, a short last range, column counts that
+    leave half a pair: against the (expert, N-tile) order bit for bit and the oracle."""
+    W1q, s1, W2q, s2 = S.moe_weights(E_, I_, K_, Nout, device=cuda_device)
+    x, ids, gw = S.moe_inputs(M, K_, topk, E_, rep=2, device=cuda_device)
+    a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=RANGE)
+    y = dg.dg_moe_w2(a, ids, gw, W2q, s2, choice=RANGE)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=CC).view(torch.int16))
+    assert torch.equal(y.view(torch.int16), dg.dg_moe_w2(a, ids, gw, W2q, s2, choice=CC).view(torch.int16))
+    if E_ <= 16:
+        r = O.moe_w1_silu(bits16(x), ids.cpu().numpy(), W1q.cpu().numpy(), s1.cpu().numpy())
+        exc = silu_excess(f64(a), r["g"], r["u"], r["absg"], r["absu"], r["a"])
+        assert (exc <= 0).all()
+        ref, bound = O.moe_w2(bits16(a), ids.cpu().numpy(), gw.cpu().numpy(), W2q.cpu().numpy(), s2.cpu().numpy())
+        assert (lin_excess(f64(y), ref, bound) <= 0).all()
+
+
+def test_moe_range_order_refuses_what_does_not_fit(cuda_device, moe_w):
+    W1q, s1, W2q, s2 = moe_w
+    M = RANGE_W2_MAX_M + 1
+    x, ids, gw = S.moe_inputs(M, K, TOPK, E, device=cuda_device)
+    a = dg.dg_moe_w1_silu(x, ids, W1q, s1, choice=RANGE)        # W1 keeps token rows: fits
+    with pytest.raises(dg.DGError):
+        dg.dg_moe_w2(a, ids, gw, W2q, s2, choice=RANGE)
+    for bad in (dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 2, 0, 0, 0, 2),      # 2 warps
+                dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 5, 0, 0, 2),      # 5 CTAs per SM
+                dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 1, 0, 2),      # params[3] must be 0
+                dg.Choice.make(dg.DG_VAR_CC_WARP, 4, 8, 0, 0, 0, 3)):     # no order 3
+        with pytest.raises(dg.DGError):
+            dg.dg_moe_w1_silu(x[:1].contiguous(), ids[:1].contiguous(), W1q, s1, choice=bad)
+
+
+@pytest.mark.parametrize("family", ["cc", "tc", "range"])
 def test_moe_invalid_ids_flag_and_zero(cuda_device, moe_w, family):
     W1q, s1, W2q, s2 = moe_w
     c = FAMILIES[family]
@@ -154,7 +213,7 @@ def test_moe_many_pairs_on_one_expert(cuda_device):
         assert (lin_excess(f64(y), ref, bound) <= 0).all(), mt
 
 
-@pytest.mark.parametrize("family", ["cc", "tc"])
+@pytest.mark.parametrize("family", ["cc", "tc", "range"])
 def test_moe_token_without_valid_slot_gives_zero(cuda_device, family):
     W1q, s1, W2q, s2 = S.moe_weights(8, 64, 256, 128, device=cuda_device)
     x, ids, gw = S.moe_inputs(2, 256, 3, 8, device=cuda_device)
@@ -166,7 +225,7 @@ def test_moe_token_without_valid_slot_gives_zero(cuda_device, family):
     assert (y[0] != 0).any()
 
 
-@pytest.mark.parametrize("family", ["cc", "tc"])
+@pytest.mark.parametrize("family", ["cc", "tc", "range"])
 def test_moe_single_expert_equals_scaled_gemv(cuda_device, family):
     """One token, one slot, gate weight 1: W2 reduces to a per-row-scaled fp8 GEMV."""
     W1q, s1, W2q, s2 = S.moe_weights(4, 512, 1024, 768, device=cuda_device)

@@ -92,12 +92,19 @@ def test_select_defaults_and_bucket_padding():
             w2 = op == dg.DG_OP_MOE_W2
             # buckets: M=5 -> 6, M=7 -> 8
             want = dg.DG_VAR_TC if ((dense_bf16 and M >= 13) or (head and M >= 2) or (w1 and M >= 7)
-                                    or (w2 and M >= 4)) else dg.DG_VAR_CC_WARP
+                                    or (w2 and M >= 5)) else dg.DG_VAR_CC_WARP
             # the warp-level tensor cores take the linear at 2-12 rows and gate/up at 3-8
             if dense_bf16 and ((2 <= M <= 12) if op == dg.DG_OP_GEMV_BF16 else (3 <= M <= 8)):
                 want = dg.DG_VAR_MMA
             assert c.variant == want and c.from_table == 0, (op, M, c)
     assert dg.dg_select(0, 129, 4096, 4096).variant == dg.DG_VAR_TC     # mid-M bucket 192
+    # MoE: the row-range order (params[5] = 2) at 1-2 rows (W1) and 1-4 rows (W2), the
+    # (expert, N-tile) order for W1 at 3-6 rows, the tensor cores above
+    order = lambda op, M: dg.dg_select(op, M, 1536 if op == dg.DG_OP_MOE_W1 else 4096,
+                                       4096 if op == dg.DG_OP_MOE_W1 else 1536).params[5]
+    assert [order(dg.DG_OP_MOE_W1, M) for M in (1, 2, 3, 6)] == [2, 2, 0, 0]
+    assert [order(dg.DG_OP_MOE_W2, M) for M in (1, 2, 3, 4)] == [2, 2, 2, 2]
+    assert dg.dg_select(dg.DG_OP_MOE_W2, 5, 4096, 1536).variant == dg.DG_VAR_TC
     with pytest.raises(dg.DGError):
         dg.dg_select(0, 513, 4096, 4096)
     # a bucket's default does not depend on where in the bucket M falls
@@ -247,6 +254,16 @@ def test_tc_split_rule_parameter_checked(tmp_path):
     assert s == 6 and "K-split rule" in why
     s, _, why = _check(_table(tmp_path, entries=ent("moe_w1_silu", [0, 1])))
     assert s == 6 and "unused tensor-core parameter" in why
+
+
+def test_moe_work_order_parameters_checked(tmp_path):
+    ent = lambda p: [{"op": "moe_w2", "M": 2, "N": 4096, "K": 1536, "pick": {"variant": 1, "params": p}}]
+    for ok in ([4, 8, 0, 64, 2, 0], [4, 8, 0, 64, 2, 1], [4, 8, 2, 0, 4, 2], [4, 4, 0, 0, 0, 2]):
+        assert _check(_table(tmp_path, entries=ent(ok)))[0] == 0, ok
+    for bad, why in (([4, 8, 0, 0, 0, 3], "work order"), ([4, 2, 0, 0, 0, 2], "row-range"),
+                     ([4, 8, 5, 0, 0, 2], "row-range"), ([4, 8, 0, 1, 0, 2], "row-range")):
+        s, _, reason = _check(_table(tmp_path, entries=ent(bad)))
+        assert s == 6 and why in reason, (bad, reason)
 
 
 def test_a8w8_select_and_argument_errors():
