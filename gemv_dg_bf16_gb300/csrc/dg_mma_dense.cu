@@ -1,5 +1,6 @@
 // dg_mma_dense.cu -- warp-level tensor-core family (DG_VAR_MMA) for the bf16 linear and
-// the fused gate/up + SiLU.mul at 3..15 token rows.
+// the fused gate/up + SiLU.mul at 1..16 token rows (the defaults: linear 2-12 rows,
+// gate/up 3-8).
 //
 // mstar PR #1104, "What changed": the decode linear picks its kernel per row count.
 // Between the CUDA-core rows (1-2 tokens: FMA issue and bf16 unpack grow with every
