@@ -11,7 +11,7 @@ the measured HBM peak) per (N,K,M); `value` is the whole step's weight bytes
 divided by its device time (GB/s).  The other hot-path workloads (the bf16 GEMV
 2048x1024 at M=1, fused gate/up, fp8 head + argmax, MoE W1/W2, mid-M rows, the A8W8
 block-scaled linear with its activation quantisation, the batch-invariant numerics
-mode at 1-2 rows, and chained gate/up -> down and W1 -> W2 pairs) are measured in the
+mode at 1-8 rows, and chained gate/up -> down and W1 -> W2 pairs) are measured in the
 same run and reported under "ops".
 
 Timing: each shape's calls are captured in a CUDA graph of R back-to-back calls
@@ -46,7 +46,7 @@ MID_NK = [(32768, 1024), (8192, 1024), (4096, 12288)]
 MOE_M = [1, 2, 4, 8, 16]
 A8_NK = [(32768, 1024), (8192, 4096)]
 A8_M = [1, 2, 4, 8, 16, 32, 64]
-INV_M = [1, 2]
+INV_M = [1, 2, 4, 8]
 MOE_E, MOE_I, MOE_K, MOE_TOPK = 128, 1536, 4096, 6
 HEAD_N, HEAD_K = 248320, 4096
 FALLBACK_HBM_GBS = 6800.0
@@ -336,8 +336,8 @@ def run_gpu(args):
                     [(lambda W=W, x=x, y=y, ws=ws, sw=sw: dg.dg_gemv_a8w8_blockscale(x, W, sw, y, ws=ws, stream=stream))
                      for W in Wa], wb, launches_per_call=2 if sep else 1)
             del Wa
-        # --- the bf16 sweep shapes at 1-2 rows in the batch-invariant numerics mode (the
-        #     tensor-core family where the fastest mode takes the CUDA cores)
+        # --- the bf16 sweep shapes at 1-8 rows in the batch-invariant numerics mode (the
+        #     tcgen05 family where the fastest mode takes the CUDA cores or mma.sync)
         if need("gemv_bf16_invariant", [{"M": M, "N": N, "K": K} for (N, K) in SWEEP_NK for M in INV_M]):
             dg.dg_set_numerics(dg.DG_NUMERICS_BATCH_INVARIANT)
             try:

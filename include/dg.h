@@ -169,9 +169,10 @@ unsigned dg_launch_flags(void);
 /* Numerics mode (process-wide); it steers dg_select, and so every call made with a
  * NULL choice.
  *   DG_NUMERICS_FASTEST (default): each row bucket takes its fastest kernel family.
- *     The CUDA-core families (1-2 rows for the linears) and the tensor-core
- *     families reduce in different orders, so a row's bits can change when the
- *     same row is computed inside a larger batch (both meet the same error bound).
+ *     The CUDA-core families (1 row for the bf16 linear, 1-2 for gate/up), the
+ *     warp-level tensor-core family (2-12 and 3-8 rows) and the tcgen05 families
+ *     reduce in different orders, so a row's bits can change when the same row is
+ *     computed inside a larger batch (all meet the same error bound).
  *   DG_NUMERICS_BATCH_INVARIANT: every bucket of an op takes one family (the
  *     tensor cores; the fp8 head with K > 8192 the CUDA cores), so output row m is
  *     a function of input row m alone -- for the MoE ops, of token m's activations,
@@ -181,7 +182,8 @@ unsigned dg_launch_flags(void);
  *     ignored in this mode; an explicit choice passed to a call is used as given.
  * The pages ask for bitwise-equal results per shape only (Strata PR #1297,
  * "Summary"; "Decode optimization round 3", "Validation"); this mode extends the
- * guarantee across row counts at the cost of the CUDA-core speed at 1-2 rows. */
+ * guarantee across row counts at the cost of the CUDA-core and warp-level speed
+ * at 1-12 rows. */
 #define DG_NUMERICS_FASTEST 0
 #define DG_NUMERICS_BATCH_INVARIANT 1
 dg_status dg_set_numerics(int mode);   /* DG_ERR_INVALID_ARG for an unknown mode */
