@@ -1,6 +1,7 @@
 // dg_tc_dense.cu -- tcgen05 tensor-core family (DG_VAR_TC) for the bf16 linear and
-// the fused gate/up + SiLU.mul (the default from three token rows up, where the
-// CUDA-core FMA and bf16-unpack work per weight byte would start to bound it).
+// the fused gate/up + SiLU.mul (the default from 13 token rows up for the linear and
+// from 9 for gate/up, where the tile is a real dense contraction), and the A8W8
+// block-scaled linear.
 //
 // Swap-AB: a CTA owns a tile of 128 weight rows (the MMA's M) and one fixed K
 // range; the tokens are the MMA's N (M padded to MP in {16, 32, 64, 128, 256};
@@ -229,17 +230,24 @@ __device__ __forceinline__ void store_staged(const TcArgs& a, const float* S, in
     }
 }
 
-template <int MP, int EPI>
+template <int MP, int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_dense_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, TcArgs a)
 {
     // EPI 2 (A8W8): e4m3 weights, 128 per stage row; the activations are quantised
     // into shared memory by the epilogue warps, so a stage holds the weight box only.
+    // PAIR (256-token tiles without a K-split, more tiles than SMs): the CTA owns two
+    // consecutive row tiles, a stage holds both weight boxes beside the one activation
+    // box they share, and two TMEM accumulators take the two MMA chains -- one wave of
+    // CTAs, each activation box loaded once for 256 weight rows.  Every tile's chain is
+    // the same as a CTA of its own would run, so the bits do not change.
     constexpr bool A8 = EPI == 2;
+    static_assert(!PAIR || (MP == 256 && !A8), "paired tiles are the 256-token bf16 path");
     constexpr int KBE = A8 ? kA8Block : kKB;      // K elements per stage
     constexpr int kXBox = A8 ? 0 : MP * kKB * 2;
-    constexpr int kStage = kWBox + kXBox;
-    constexpr uint32_t kCols = A8 ? static_cast<uint32_t>(kA8Bufs * MP) : (MP < 32 ? 32 : MP);
+    constexpr int kWBoxes = PAIR ? 2 : 1;
+    constexpr int kStage = kWBox * kWBoxes + kXBox;
+    constexpr uint32_t kCols = A8 ? static_cast<uint32_t>(kA8Bufs * MP) : (PAIR ? 2 * MP : (MP < 32 ? 32 : MP));
     constexpr uint32_t kIdesc = A8 ? tc::idesc_f8(MP) : tc::idesc_bf16(MP);
     constexpr int kExtraBars = A8 ? kA8Bars : 0;
 
@@ -261,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool clustered = a.nsplit > 1;
     // the parked partial tile takes the padded stride when the idle ring holds it
     const int pstride = static_cast<size_t>(S) * kStage >= static_cast<size_t>(MP) * kPStride * 4 ? kPStride : kTileRows;
-    const int tile = blockIdx.x / a.nsplit;
+    const int tile = PAIR ? 2 * static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) / a.nsplit;
+    const int ntiles_here = PAIR ? (tile + 1 < a.tiles ? 2 : 1) : 1;
     const int split = clustered ? static_cast<int>(cluster_rank()) : 0;
     const int kb0 = static_cast<int>((static_cast<long long>(split) * a.nkb) / a.nsplit);
     const int kb1 = static_cast<int>((static_cast<long long>(split + 1) * a.nkb) / a.nsplit);
@@ -313,11 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = tc::su32(smem + i * kStage);
                 tc::bar_expect_tx(full0 + 8 * i, kStage);
                 tc::tma_2d_hint(dst, &tmW, (kb0 + i) * KBE, tile * kTileRows, full0 + 8 * i, once);
+                if constexpr (PAIR)        // (rows past N read as zeros when the tile is the last, odd one)
+                    tc::tma_2d_hint(dst + kWBox, &tmW, (kb0 + i) * KBE, (tile + 1) * kTileRows, full0 + 8 * i, once);
             }
             pdl_wait();
             if constexpr (!A8)
                 for (int i = 0; i < pre; ++i)
-                    tc::tma_2d(tc::su32(smem + i * kStage) + kWBox, &tmX, (kb0 + i) * kKB, 0, full0 + 8 * i);
+                    tc::tma_2d(tc::su32(smem + i * kStage) + kWBox * kWBoxes, &tmX, (kb0 + i) * kKB, 0, full0 + 8 * i);
             if constexpr (A8)
                 if (a.preq)
                     // every block's codes at once (rows M..MP-1 read as zeros), each
@@ -335,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::bar_expect_tx(full0 + 8 * s, kStage);
                 const int k = (kb0 + i) * KBE;
                 tc::tma_2d_hint(dst, &tmW, k, tile * kTileRows, full0 + 8 * s, once);
-                if constexpr (!A8) tc::tma_2d(dst + kWBox, &tmX, k, 0, full0 + 8 * s);
+                if constexpr (PAIR) tc::tma_2d_hint(dst + kWBox, &tmW, k, (tile + 1) * kTileRows, full0 + 8 * s, once);
+                if constexpr (!A8) tc::tma_2d(dst + kWBox * kWBoxes, &tmX, k, 0, full0 + 8 * s);
             }
         } else {
             pdl_wait();
@@ -366,11 +378,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::commit(accf0 + 8 * b);
                 } else {
                     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                    const uint32_t xa = wa + kWBox;
+                    const uint32_t xa = wa + kWBox * kWBoxes;
 #pragma unroll
                     for (int kk = 0; kk < kKB / 16; ++kk)
                         tc::mma_bf16(tmem, tc::sw128_desc(wa + kk * 32), tc::sw128_desc(xa + kk * 32), kIdesc,
                                      (i > 0 || kk > 0) ? 1u : 0u);
+                    if constexpr (PAIR)
+#pragma unroll
+                        for (int kk = 0; kk < kKB / 16; ++kk)
+                            tc::mma_bf16(tmem + static_cast<uint32_t>(MP), tc::sw128_desc(wa + kWBox + kk * 32),
+                                         tc::sw128_desc(xa + kk * 32), kIdesc, (i > 0 || kk > 0) ? 1u : 0u);
                     tc::commit(empty0 + 8 * s);
                 }
             }
@@ -522,20 +539,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!good && row == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
         if (!clustered) {
             // Stage the tile S[t][row] (fp32) in the now idle stage memory, then write
-            // it out in coalesced 16-byte pieces.
+            // it out in coalesced 16-byte pieces (paired tiles: one after the other).
             float* S = reinterpret_cast<float*>(smem);
-            if (good) {
 #pragma unroll 1
-                for (int c = 0; c < MP / 16 && c * 16 < a.M; ++c) {
-                    uint32_t v[16];
-                    tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c * 16, v);
+            for (int pt = 0; pt < ntiles_here; ++pt) {
+                if (pt > 0) asm volatile("bar.sync 1, 128;" ::: "memory");     // S is free again
+                if (good) {
+#pragma unroll 1
+                    for (int c = 0; c < MP / 16 && c * 16 < a.M; ++c) {
+                        uint32_t v[16];
+                        tc::tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(pt * MP + c * 16), v);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (c * 16 + j < a.M) S[(c * 16 + j) * kTileRows + row] = __uint_as_float(v[j]);
+                        for (int j = 0; j < 16; ++j)
+                            if (c * 16 + j < a.M) S[(c * 16 + j) * kTileRows + row] = __uint_as_float(v[j]);
+                    }
                 }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                if (good) store_staged<EPI>(a, S, kTileRows, tile + pt, 0, kTileRows, threadIdx.x - 64);
             }
-            asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (good) store_staged<EPI>(a, S, kTileRows, tile, 0, kTileRows, threadIdx.x - 64);
         } else if (a.push) {
             // Push row `row` of this rank's partial tile (tokens 0..mq-1) into the
             // shared memory of the rank that folds it.
@@ -696,7 +717,7 @@ bool encode_2d(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, 
 template <int MP, int EPI>
 const void* tc_fn()
 {
-    return reinterpret_cast<const void*>(&tc_dense_kernel<MP, EPI>);
+    return reinterpret_cast<const void*>(&tc_dense_kernel<MP, EPI, false>);
 }
 
 const void* tc_lookup(int mp, int epi)
@@ -718,6 +739,19 @@ const void* tc_lookup(int mp, int epi)
     default: return nullptr;
     }
 }
+
+// The paired-tile 256-token kernels (bf16 linear, gate/up).
+const void* tc_lookup_pair(int epi)
+{
+    return epi == 0 ? reinterpret_cast<const void*>(&tc_dense_kernel<256, 0, true>)
+                    : reinterpret_cast<const void*>(&tc_dense_kernel<256, 1, true>);
+}
+
+size_t stage_bytes_pair() { return 2 * static_cast<size_t>(kWBox) + static_cast<size_t>(256) * kKB * 2; }
+
+// Paired 256-token tiles: 3 stages of 64 KB (the epilogue stages a 128 KB tile in them).
+constexpr int kPairStages = 3;
+size_t smem_bytes_pair(int stages) { return 1024 + stages * stage_bytes_pair() + (2 * stages + 2) * 8 + 16; }
 
 size_t stage_bytes(int mp) { return kWBox + static_cast<size_t>(mp) * kKB * 2; }
 
@@ -789,10 +823,44 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
     }
     const int mp = tc_mp(M);
     const int epi = gate_up ? 1 : 0;
-    const void* fn = tc_lookup(mp, epi);
-    if (!fn) return DG_ERR_BAD_VARIANT;
     if (c.params[1] != 0 && c.params[1] != 1) return DG_ERR_BAD_VARIANT;
     const int ns = tc_nsplit(N, K, M, c.params[1] == 1);
+    const int tiles = (N + kTileRows - 1) / kTileRows;
+    // 256-token tiles without a K-split and more tiles than SMs: two tiles per CTA, one
+    // wave (the same MMA chains, so the same bits).
+    const bool pair = mp == 256 && ns == 1 && tiles > dev->sm_count;
+    const void* fn = pair ? tc_lookup_pair(epi) : tc_lookup(mp, epi);
+    if (!fn) return DG_ERR_BAD_VARIANT;
+    if (pair) {
+        const int st = c.params[0] > 0 ? c.params[0] : kPairStages;
+        const size_t smem = smem_bytes_pair(st);
+        if (st < 2 || st > 8 || smem > kMaxDynSmem) return DG_ERR_BAD_VARIANT;
+        if (ws_bytes < tc_workspace_bytes(M, N, K)) return DG_ERR_WORKSPACE_TOO_SMALL;
+        TcArgs a{};
+        a.N = N;
+        a.K = K;
+        a.M = M;
+        a.tiles = tiles;
+        a.nkb = (K + kKB - 1) / kKB;
+        a.nsplit = 1;
+        a.mq = (M + 3) & ~3;
+        a.slice_max = slice_max(1);
+        a.stages = st;
+        a.out = static_cast<uint16_t*>(out);
+        a.ld_out = ld_out;
+        a.ws = static_cast<uint8_t*>(ws);
+        CUtensorMap tmW, tmX;
+        if (!encode_2d(&tmW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kKB, kTileRows) ||
+            !encode_2d(&tmX, x, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kKB, 256u))
+            return DG_ERR_CUDA;
+        if (occupancy(fn, kThreads, smem) < 1) return DG_ERR_UNSUPPORTED_SHAPE;
+        void* args[] = {&tmW, &tmX, &a};
+        if (launch_kernel(fn, static_cast<unsigned>((tiles + 1) / 2), kThreads, smem, stream, args) != cudaSuccess) {
+            cudaGetLastError();
+            return DG_ERR_CUDA;
+        }
+        return DG_OK;
+    }
     const int mq = (M + 3) & ~3;
     // K-split fold: ranks push their rows to the folding rank (st.async) for up to 8
     // tokens when the receive buffer costs no pipeline stage; otherwise each rank

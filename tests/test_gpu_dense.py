@@ -284,6 +284,55 @@ def test_gemv_mid_m_tc_variants_bitwise_identical(cuda_device, M, N, K):
     _lin_check(x, W, yc, rows=sample_rows(N, 32, seed=M))
 
 
+# 256-token tiles on more tiles than SMs run two tiles per CTA (one wave); 153 tiles
+# gives an odd last CTA, +40 rows a partial last tile.
+PAIR_N = [128 * 153, 128 * 153 + 40]
+
+
+@pytest.mark.parametrize("K", [64, 1040])
+@pytest.mark.parametrize("N", PAIR_N)
+@pytest.mark.parametrize("M", [129, 256, 300])
+def test_gemv_mid_m_paired_tiles(cuda_device, M, N, K):
+    """Paired tiles against the oracle (rows of the odd last CTA included), against one
+    tile per CTA bit for bit (the first 152 tiles alone take that path with the same
+    unsplit chain, for the first 256 token rows), and across pipeline depths."""
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    y = dg.dg_gemv_bf16(x, W)
+    rows = np.unique(np.concatenate([sample_rows(N, 40, seed=N + K + M), np.arange(N - 130, N)]))
+    torch.cuda.synchronize()
+    _lin_check(x, W, y, rows=rows)
+    n1 = 128 * 152
+    y1 = dg.dg_gemv_bf16(x, W[:n1].contiguous())
+    m1 = min(M, 256)          # (rows past 256 are a second chunk of fewer tokens, with its own split rule)
+    assert torch.equal(y[:m1, :n1].contiguous().view(torch.int16), y1[:m1].contiguous().view(torch.int16))
+    for st in (2, 3):
+        y2 = dg.dg_gemv_bf16(x, W, choice=dg.Choice.make(dg.DG_VAR_TC, st))
+        assert torch.equal(y2.view(torch.int16), y.view(torch.int16)), st
+
+
+def test_gemv_mid_m_paired_tiles_one_hot_exact(cuda_device):
+    """x = e_k rows: every output of both tiles of every CTA equals W[n, k] exactly."""
+    N, K, M = 128 * 153 + 40, 1040, 256
+    _, W = S.linear_inputs(1, N, K, device=cuda_device)
+    ks = [(37 * m + 5) % K for m in range(M)]
+    x = torch.zeros((M, K), dtype=torch.bfloat16, device=cuda_device)
+    for m, k in enumerate(ks):
+        x[m, k] = 1.0
+    y = dg.dg_gemv_bf16(x, W)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), W[:, ks].t().contiguous().view(torch.int16))
+
+
+@pytest.mark.parametrize("M", [129, 256])
+def test_gate_up_mid_m_paired_tiles(cuda_device, M):
+    Nh = 64 * 153 + 20                 # 2 * Nh = 19624 rows: 154 tiles
+    x, Wgu = S.gate_up_inputs(M, Nh, 1040, device=cuda_device)
+    out = dg.dg_gate_up_silu(x, Wgu)
+    torch.cuda.synchronize()
+    cols = np.unique(np.concatenate([sample_rows(Nh, 40, seed=M), np.arange(Nh - 70, Nh)]))
+    _gate_up_check(x, Wgu, out, cols=cols)
+
+
 @pytest.mark.parametrize("M", [160, 384])
 def test_gate_up_mid_m(cuda_device, M):
     x, Wgu = S.gate_up_inputs(M, 700, 2056, device=cuda_device)
