@@ -29,11 +29,11 @@ size_t moe_range_smem(bool w1, int M, int topk, int K, int rpc);
 
 // tcgen05 family (dg_tc_dense.cu): padded token count, fixed K-split of a shape,
 // workspace bytes, and the launcher (bf16 linear or interleaved gate/up rows).
+struct DeviceInfo;
 int tc_mp(int M);
-int tc_nsplit(int N, int K, int M, bool fixed);
+int tc_nsplit(const DeviceInfo* dev, int N, int K, int M, bool fixed);
 size_t tc_workspace_bytes(int M, int N, int K);
 
-struct DeviceInfo;
 dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W,
                     void* out, int M, int N, int K, int ld_out, void* ws, size_t ws_bytes, cudaStream_t stream);
 
@@ -45,7 +45,7 @@ dg_status launch_mw(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
 // A8W8 block-scaled linear on the tcgen05 family (dg_tc_dense.cu): the fixed K-split
 // of a shape and the launcher; the activation quantisation alone (dg_a8.cu).
 constexpr int kA8MaxRows = 64;
-int tc_a8_nsplit(int N, int K);
+int tc_a8_nsplit(const DeviceInfo* dev, int N, int K);
 size_t a8_workspace_bytes(int M, int K);
 dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x, const void* Wq, const float* sw,
                        void* y, int M, int N, int K, void* ws, size_t ws_bytes, cudaStream_t stream);

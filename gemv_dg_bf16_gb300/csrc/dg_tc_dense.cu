@@ -779,19 +779,79 @@ int default_stages(int mp, size_t recv)
 
 int tc_mp(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256))); }
 
-int tc_nsplit(int N, int K, int M, bool fixed)
+namespace {
+
+// Never launched: stands in for a tensor-core CTA (same block, same dynamic shared
+// memory) in the cluster-residency query below.  For the tcgen05 kernels themselves
+// the driver's occupancy answer is one CTA per SM at any shared memory size, yet
+// their launches hold two per SM at up to 112 KB each (timed on GB300: a K-split
+// pays a second wave only once its clusters outnumber the two-per-SM capacity).
+__global__ void __launch_bounds__(kThreads, 1) cluster_slot_kernel() {}
+
+// Clusters of `size` tensor-core CTAs that are resident at once with two CTAs per SM
+// (up to 128 tokens) or one (256-token tiles).  A cluster's CTAs share one GPC, so
+// where the GPCs do not divide evenly this is below SMs x CTAs-per-SM / size: on
+// GB300 (152 SMs), one CTA per SM holds 15 clusters of 8, 23 of 6 and 46 of 3.
+int cluster_capacity(const DeviceInfo* dev, bool two_per_sm, int size)
+{
+    static std::mutex mu;
+    static int cap[64][2][kMaxCluster + 1];
+    static bool attr_set = false;
+    const int fallback = (two_per_sm ? 2 : 1) * dev->sm_count / size;
+    if (size < 1 || size > kMaxCluster || dev->device < 0 || dev->device >= 64) return fallback;
+    std::lock_guard<std::mutex> lk(mu);
+    int& c = cap[dev->device][two_per_sm ? 1 : 0][size];
+    if (c == 0) {
+        const void* fn = reinterpret_cast<const void*>(&cluster_slot_kernel);
+        if (!attr_set) {
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxDynSmem));
+            attr_set = true;
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(size * dev->sm_count));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = two_per_sm ? smem_bytes(128, default_stages(128, 0), 0) : smem_bytes(256, kWideStages, 0);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = static_cast<unsigned>(size);
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+        c = n > 0 ? n : fallback;
+    }
+    return c;
+}
+
+}  // namespace
+
+int tc_nsplit(const DeviceInfo* dev, int N, int K, int M, bool fixed)
 {
     const int tiles = (N + kTileRows - 1) / kTileRows;
     const int nkb = (K + kKB - 1) / kKB;
     // Up to 128 tokens two CTAs share an SM: the split fills both slots of every SM
-    // (at most 304 CTAs, one wave; measured on GB300 6-11 % faster than about 160
-    // CTAs on the 64-100 MB shapes, where a few doubled-up SMs set the pace).
-    // 256-token tiles take one SM each, so their split keeps the grid within 152.  A
-    // fixed split takes the first rule at every row count, so a row's bits do not
+    // (measured on GB300 6-11 % faster than about 160 CTAs on the 64-100 MB shapes,
+    // where a few doubled-up SMs set the pace).  256-token tiles take one SM each.  A
+    // fixed split plans for two CTAs per SM at every row count, so a row's bits do not
     // depend on how many rows share the call.
-    int ns = (fixed || tc_mp(M) <= 128) ? 304 / tiles : 152 / tiles;
+    const bool two = fixed || tc_mp(M) <= 128;
+    int ns = (two ? 2 : 1) * dev->sm_count / tiles;
     if (ns > kMaxCluster) ns = kMaxCluster;
-    if (ns > nkb) ns = nkb;
+    // At least 4 K-blocks (256 elements) per rank: with less the fold costs more than
+    // the streaming it shares (K = 1024 at 128 tokens: 4 ranks 8-18 % faster than 8).
+    if (ns > nkb / 4) ns = nkb / 4;
+    // One wave: every cluster resident at once.  A split one rank too wide for the
+    // GPCs runs a second wave of clusters (2048x4096 at 256 tokens: 8 ranks 26.9 us,
+    // 6 ranks 15.7 us).
+    while (ns > 1 && tiles > cluster_capacity(dev, two, ns)) --ns;
+    // 256-token tiles: a 2-rank fold of a 128 KB partial costs more than halving a
+    // rank's stream of at most 32 K-blocks (8192x1024: 16.6 us split, 13.4 us whole).
+    if (!two && ns == 2 && nkb <= 32) ns = 1;
     if (ns < 1) ns = 1;
     return ns;
 }
@@ -824,7 +884,7 @@ dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, con
     const int mp = tc_mp(M);
     const int epi = gate_up ? 1 : 0;
     if (c.params[1] != 0 && c.params[1] != 1) return DG_ERR_BAD_VARIANT;
-    const int ns = tc_nsplit(N, K, M, c.params[1] == 1);
+    const int ns = tc_nsplit(dev, N, K, M, c.params[1] == 1);
     const int tiles = (N + kTileRows - 1) / kTileRows;
     // 256-token tiles without a K-split and more tiles than SMs: two tiles per CTA, one
     // wave (the same MMA chains, so the same bits).
@@ -924,14 +984,16 @@ namespace dg {
 
 // ------------------------------------------------------------------ A8W8 blockscale
 
-int tc_a8_nsplit(int N, int K)
+int tc_a8_nsplit(const DeviceInfo* dev, int N, int K)
 {
     const int tiles = (N + kTileRows - 1) / kTileRows;
     const int nkb = (K + kA8Block - 1) / kA8Block;
-    // Both CTA slots of every SM (at most 304 CTAs), and at most 8 K-blocks of quantised
-    // activations per rank (64 KB at 64 tokens); a function of the shape alone, so a
-    // row's bits do not depend on how many rows share the call.
-    int ns = 304 / tiles;
+    // Both CTA slots of every SM, in one wave of clusters, and at most 8 K-blocks of
+    // quantised activations per rank (64 KB at 64 tokens); a function of the shape
+    // alone, so a row's bits do not depend on how many rows share the call.
+    int ns = 2 * dev->sm_count / tiles;
+    if (ns > kMaxCluster) ns = kMaxCluster;
+    while (ns > 1 && tiles > cluster_capacity(dev, true, ns)) --ns;
     const int by_smem = (nkb + 7) / 8;
     if (ns < by_smem) ns = by_smem;
     if (ns > kMaxCluster) ns = kMaxCluster;
@@ -971,7 +1033,7 @@ dg_status launch_tc_a8(const DeviceInfo* dev, const dg_choice& c, const void* x,
     const int mp = tc_mp(M);
     const void* fn = tc_lookup(mp, 2);
     if (!fn) return DG_ERR_BAD_VARIANT;
-    const int ns = tc_a8_nsplit(N, K);
+    const int ns = tc_a8_nsplit(dev, N, K);
     const int nkb = (K + kA8Block - 1) / kA8Block;
     const int xq_blocks = (nkb + ns - 1) / ns;
     if (xq_blocks > kA8MaxBlocks) return DG_ERR_UNSUPPORTED_SHAPE;
