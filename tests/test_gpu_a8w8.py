@@ -93,6 +93,20 @@ def test_a8w8_variants_bitwise_identical(cuda_device, M, N, K):
             assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), (st, pq)
 
 
+@pytest.mark.parametrize("tiles", [7, 38, 42, 48, 60, 100])
+@pytest.mark.parametrize("M", [16, 64])
+def test_a8w8_every_split_width(cuda_device, M, tiles):
+    """The A8W8 K-split at the tile counts where one wave of clusters sets its width,
+    against the oracle on sampled rows."""
+    N, K = 128 * tiles - 40, 4096
+    x, Wq, sw = S.a8w8_inputs(M, N, K, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GEMV_A8W8, M, N, K)
+    y = dg.dg_gemv_a8w8_blockscale(x, Wq, sw, ws=ws)
+    torch.cuda.synchronize()
+    assert dg.dg_device_status(ws) == 0
+    _check(x, Wq, sw, y, rows=sample_rows(N, 24, seed=N + M))
+
+
 @pytest.mark.parametrize("N,K", [(8192, 4096), (300, 1040)])
 def test_a8w8_rows_independent_of_the_batch(cuda_device, N, K):
     """The K-split is fixed by (N, K), so a row's bits do not depend on M or on the

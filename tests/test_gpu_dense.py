@@ -286,6 +286,30 @@ def test_gemv_mid_m_tc_variants_bitwise_identical(cuda_device, M, N, K):
 
 # 256-token tiles on more tiles than SMs run two tiles per CTA (one wave); 153 tiles
 # gives an odd last CTA, +40 rows a partial last tile.
+# Tile counts at which the tensor-core K-split takes each cluster width from 1 to 8 ranks,
+# including the counts where one wave of clusters caps it below SMs x CTAs per SM / tiles
+# (37-38, 39-43, 47-50, 59-60, 75-76, 98-101 tiles at two CTAs per SM; 16 and 24 tiles at
+# one), the last tile ragged.
+SPLIT_TILES = [1, 3, 5, 7, 16, 24, 38, 43, 48, 60, 76, 100]
+
+
+@pytest.mark.parametrize("K", [1024, 4096 + 64])
+@pytest.mark.parametrize("tiles", SPLIT_TILES)
+@pytest.mark.parametrize("M", [16, 100, 200])
+def test_gemv_tc_every_split_width(cuda_device, M, tiles, K):
+    """The tensor-core linear at every K-split width the rule picks (one per tile count
+    above), against the oracle on sampled rows, and bit for bit across ring depths."""
+    N = 128 * tiles - 24
+    x, W = S.linear_inputs(M, N, K, device=cuda_device)
+    ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K)
+    y = dg.dg_gemv_bf16(x, W, ws=ws, choice=TC)
+    torch.cuda.synchronize()
+    assert dg.dg_device_status(ws) == 0
+    _lin_check(x, W, y, rows=sample_rows(N, 24, seed=N + K + M))
+    y3 = dg.dg_gemv_bf16(x, W, choice=dg.Choice.make(dg.DG_VAR_TC, 3))
+    assert torch.equal(y3.view(torch.int16), y.view(torch.int16))
+
+
 PAIR_N = [128 * 153, 128 * 153 + 40]
 
 
