@@ -810,7 +810,7 @@ int cluster_capacity(const DeviceInfo* dev, bool two_per_sm, int size)
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(size * dev->sm_count));
         cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = two_per_sm ? smem_bytes(128, default_stages(128, 0), 0) : smem_bytes(256, kWideStages, 0);
+        cfg.dynamicSmemBytes = two_per_sm ? kCoResidentSmem : smem_bytes(256, kWideStages, 0);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = static_cast<unsigned>(size);
