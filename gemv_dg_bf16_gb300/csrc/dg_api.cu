@@ -251,6 +251,7 @@ dg_status dg_init(int device)
         g_dev_ok[device] = true;
     }
     if (first) {
+        tc_capacity_init(&info);
         const char* path = std::getenv("DG_TABLE");
         if (path && *path) dg_table_load(path);   // refusal prints one line; defaults stay
     }

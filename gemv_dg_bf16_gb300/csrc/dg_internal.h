@@ -32,6 +32,10 @@ size_t moe_range_smem(bool w1, int M, int topk, int K, int rpc);
 struct DeviceInfo;
 int tc_mp(int M);
 int tc_nsplit(const DeviceInfo* dev, int N, int K, int M, bool fixed);
+// Queries (once per device, from dg_init) how many thread-block clusters of each size
+// the tensor-core kernels can keep resident, so that no launch -- inside a stream
+// capture or not -- queries the driver for its K-split.
+void tc_capacity_init(const DeviceInfo* dev);
 size_t tc_workspace_bytes(int M, int N, int K);
 
 dg_status launch_tc(bool gate_up, const DeviceInfo* dev, const dg_choice& c, const void* x, const void* W,

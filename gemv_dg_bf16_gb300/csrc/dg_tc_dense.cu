@@ -830,6 +830,14 @@ int cluster_capacity(const DeviceInfo* dev, bool two_per_sm, int size)
 
 }  // namespace
 
+void tc_capacity_init(const DeviceInfo* dev)
+{
+    for (int size = 1; size <= kMaxCluster; ++size) {
+        cluster_capacity(dev, true, size);
+        cluster_capacity(dev, false, size);
+    }
+}
+
 int tc_nsplit(const DeviceInfo* dev, int N, int K, int M, bool fixed)
 {
     const int tiles = (N + kTileRows - 1) / kTileRows;

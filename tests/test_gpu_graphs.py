@@ -229,3 +229,41 @@ def test_chained_mlp_pair_in_graph_matches_separate_calls(cuda_device, M):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+
+
+_FIRST_CALL_CAPTURED = r"""
+import sys, torch
+sys.path.insert(0, ROOT)
+import gemv_dg_bf16_gb300 as dg
+from synth import decode_inputs as S
+dg.dg_init(0)
+dev = torch.device("cuda:0")
+out = []
+for (M, N, K) in [(16, 4096, 4096), (200, 2048, 4096), (64, 6144, 4096)]:
+    x, W = S.linear_inputs(M, N, K, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    ws = dg.workspace(dg.DG_OP_GEMV_BF16, M, N, K, device=dev)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):      # this shape's first call is the captured one
+        dg.dg_gemv_bf16(x, W, y, ws=ws, choice=dg.Choice.make(dg.DG_VAR_TC, 0), stream=s)
+    g.replay()
+    torch.cuda.synchronize()
+    eager = dg.dg_gemv_bf16(x, W, choice=dg.Choice.make(dg.DG_VAR_TC, 0))
+    torch.cuda.synchronize()
+    out.append(bool(torch.equal(y.view(torch.int16), eager.view(torch.int16))))
+print(out)
+"""
+
+
+def test_first_tensor_core_call_inside_a_capture():
+    """In a fresh process, the first tensor-core calls (K-split clusters of 8, 6 and 5
+    ranks) are made inside a stream capture: the replay gives the eager call's bits, so
+    the launch took the same split as outside a capture."""
+    import os, subprocess, sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = "ROOT = %r\n" % root + _FIRST_CALL_CAPTURED
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600, cwd=root)
+    assert res.returncode == 0, res.stderr[-2000:]
+    assert res.stdout.strip().splitlines()[-1] == "[True, True, True]", res.stdout + res.stderr[-2000:]
