@@ -16,8 +16,9 @@ same run and reported under "ops".
 
 Timing: each shape's calls are captured in a CUDA graph of R back-to-back calls
 that rotate over enough weight copies to exceed 3x the L2 size (so no call finds
-its weights in L2); the graph is replayed once per step between CUDA events on the
-capturing stream; per-call time = event time / R.
+its weights in L2; up to 16 copies their count is a power of two, so consecutive
+graphs over the same copies continue the rotation); the graph is replayed once per
+step between CUDA events on the capturing stream; per-call time = event time / R.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -162,7 +163,14 @@ def _graph_case(torch, calls, reps: int, stream):
 
 
 def _copies_for(nbytes: int, l2: int) -> int:
-    return max(2, -(-3 * l2 // max(1, nbytes)))
+    """Weight copies for one shape: at least 3x L2 of them.  Up to 16 copies the count is
+    rounded up to a power of two, so that a graph of 16 calls makes whole rotations and
+    the next graph over the same copies (the next row count) starts on the copy used
+    longest ago, not on one a few calls old that may still sit in L2."""
+    n = max(2, -(-3 * l2 // max(1, nbytes)))
+    if n <= 16:
+        n = 1 << (n - 1).bit_length()
+    return n
 
 
 def run_gpu(args):
