@@ -80,6 +80,25 @@ cudaError_t launch_kernel(const void* fn, unsigned grid, unsigned block, size_t 
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+cudaError_t launch_kernel_cooperative(const void* fn, unsigned grid, unsigned block, size_t smem,
+                                      cudaStream_t stream, void** args)
+{
+    if (t_check_only) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 int occupancy(const void* fn, int threads, size_t smem)
 {
     std::lock_guard<std::mutex> lk(g_mu);

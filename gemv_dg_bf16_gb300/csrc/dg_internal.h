@@ -102,6 +102,10 @@ int occupancy(const void* fn, int threads, size_t smem);
 bool pdl_enabled();
 cudaError_t launch_kernel(const void* fn, unsigned grid, unsigned block, size_t smem, cudaStream_t stream,
                           void** args);
+// The same as a cooperative launch: the runtime starts it only with every CTA resident
+// at once, whatever else the GPU runs -- for kernels with a grid-wide barrier.
+cudaError_t launch_kernel_cooperative(const void* fn, unsigned grid, unsigned block, size_t smem,
+                                      cudaStream_t stream, void** args);
 
 // While an instance lives, launch_kernel on this thread checks nothing more and
 // launches nothing (returns success): an entry point run under it performs every

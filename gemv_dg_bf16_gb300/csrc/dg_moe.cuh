@@ -205,8 +205,8 @@ __device__ inline void route_scan(Route& R, const int32_t* __restrict__ ids, int
 }
 
 // Sense-reversing grid barrier for a grid whose CTAs are all resident at once (a
-// persistent grid sized by the occupancy; a dependent launch starts only after
-// every CTA of this one has started, so none of them can be kept off an SM by it).
+// persistent grid sized by the occupancy and launched cooperatively, so that no other
+// kernel, of this stream or another, can keep one of them off an SM).
 // Counter at bar[0], generation at bar[1]; the last arriver resets the counter for
 // the next call.  One thread per CTA calls it.  Bounded: false after 2 s, or at
 // once when `abort_flag` (if given) is raised.

@@ -13,8 +13,9 @@
 //   W1 tile: 64 gate rows j0.. and the 64 matching up rows I + j0.. (two TMA boxes);
 //            a[t, k, j] = bf16(silu(g * s1[e, j]) * (u * s1[e, I + j]))
 //   W2 tile: 128 output rows n0..; (h * s2[e, n]) * gw[t, k] go to the workspace;
-//            after one grid barrier (the grid is one resident CTA per SM) every
-//            CTA folds a share of the outputs over the valid slots in slot order.
+//            after one grid barrier (one CTA per SM, launched cooperatively so all
+//            are resident at once) every CTA folds a share of the outputs over the
+//            valid slots in slot order.
 //   warp 0     TMA producer (weights only, ring of stages)
 //   warp 1     TMEM allocation, MMA issue (lane 0)
 //   warps 2-5  split activations for each pass, epilogue of each tile
@@ -281,10 +282,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = et; j < a.I; j += 128) a.out[static_cast<size_t>(i) * a.I + j] = 0;
         } else {
             // Combine: once every CTA has written its terms (one grid barrier; the grid
-            // is one CTA per SM, and a dependent launch starts only after all of them
-            // have started, so all are resident), the outputs are folded in slot order,
-            // spread over every CTA's epilogue threads.  Tokens without a valid slot
-            // get y = 0.
+            // is one CTA per SM and the launch is cooperative, so all are resident), the
+            // outputs are folded in slot order, spread over every CTA's epilogue
+            // threads.  Tokens without a valid slot get y = 0.
             __threadfence();
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (et == 0) grid_ok = grid_barrier(reinterpret_cast<unsigned*>(a.ws + kWsGridBarrier), abort_flag) ? 1 : 0;
@@ -304,8 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     a.out[static_cast<size_t>(t) * a.Nout + n] = f32_to_bf16_bits(y);
                 }
-            } else if (et == 0) {
-                set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
+            } else {
+                // The barrier gave up: this CTA's share of y becomes NaN rather than
+                // keeping an earlier call's values, beside the status word.
+                const long total = static_cast<long>(a.M) * a.Nout;
+                for (long i = static_cast<long>(blockIdx.x) * 128 + et; i < total; i += static_cast<long>(gridDim.x) * 128)
+                    a.out[i] = 0x7FC0u;
+                if (et == 0) set_status(a.ws, DG_DEVERR_WAIT_TIMEOUT);
             }
         }
     }
@@ -369,7 +374,12 @@ dg_status launch_tc_moe(bool w1, const DeviceInfo* dev, const dg_choice& c, cons
     const size_t smem = smem_bytes(nkb, stages);
     if (occupancy(fn, kThreads, smem) < 1) return DG_ERR_UNSUPPORTED_SHAPE;
     void* args[] = {&tm, &A};
-    if (launch_kernel(fn, static_cast<unsigned>(dev->sm_count), kThreads, smem, stream, args) != cudaSuccess) {
+    // W2 combines after a grid-wide barrier: launched cooperatively, so all its CTAs are
+    // resident at once even when other streams' kernels hold SMs.
+    const cudaError_t le = w1 ? launch_kernel(fn, static_cast<unsigned>(dev->sm_count), kThreads, smem, stream, args)
+                              : launch_kernel_cooperative(fn, static_cast<unsigned>(dev->sm_count), kThreads, smem,
+                                                          stream, args);
+    if (le != cudaSuccess) {
         cudaGetLastError();
         return DG_ERR_CUDA;
     }

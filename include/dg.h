@@ -36,7 +36,9 @@
  *   allocated (e.g. cudaMemsetAsync); every call leaves its counters at zero
  *   again (a grid barrier's generation word keeps counting; any value is fine).
  *   Calls that share one workspace must be ordered on one stream.  After a
- *   DG_DEVERR_WAIT_TIMEOUT the workspace must be zero-filled again.
+ *   DG_DEVERR_WAIT_TIMEOUT the workspace must be zero-filled again, and the
+ *   outputs of the call that set it are not valid (where a grid-wide combine
+ *   gave up, the tensor-core MoE W2 writes NaN rather than leave older values).
  *   The first 16 bytes hold a sticky device status word (dg_device_status).
  * - `choice` may be NULL (dg_select picks); otherwise the given variant runs.
  * - Accumulation is fp32 in a fixed order that does not depend on the kernel
