@@ -376,7 +376,8 @@ dg_status dg_table_check(const char* path, const char* arch, int driver_version,
  * each candidate's output with the compiled default's on the same inputs, and
  * write a table that keeps every candidate's time and parameters beside the pick.
  * A candidate replaces the default only if it is bitwise equal and at least 2 %
- * faster.  mstar PR #1104, "What changed" (the promotion rule, every candidate's
+ * faster, first in the sweep and then in the medians of three more timings of
+ * each, taken alternately (pick_us / default_us are then those medians).  mstar PR #1104, "What changed" (the promotion rule, every candidate's
  * time kept beside the choice); Strata PR #1297, "Summary" (byte-compared
  * variants only) and "True-default baseline"; "Decode optimization round 3",
  * "Rejected paths" (re-measure every row against the incumbent in context).
