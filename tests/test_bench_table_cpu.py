@@ -53,3 +53,25 @@ def test_table_report_compares_the_same_shapes():
     # 16000 bytes in 17 us with the defaults
     assert r["defaults_value"] == pytest.approx(16000 / 17e-6 / 1e9, abs=0.05)
     assert [(s["M"], s["us_table"], s["us_default"]) for s in r["shapes"]] == [(1, 7.0, 7.0), (2, 9.0, 10.0)]
+
+
+@pytest.mark.parametrize("wb_mb", [4.2, 16.8, 33.6, 67.1, 100.7, 201.3, 1017.1])
+def test_weight_copies_defeat_l2_across_consecutive_graphs(wb_mb):
+    """A graph of R calls rotates over the copies; the next graph over the same copies
+    (the next row count) starts again at copy 0.  With at most R copies every call's copy
+    was last used at least 3x L2 of other weights earlier, inside a graph and across the
+    seam; with more copies than calls (matrices under 3x L2 / R) a graph uses its first R
+    copies, all distinct."""
+    l2, R = 126 * 2 ** 20, 16
+    wb = int(wb_mb * 1e6)
+    n = bench._copies_for(wb, l2)
+    assert n >= 2 and n * wb >= 3 * l2
+    seq = [i % n for i in range(R)] * 3                      # three graphs back to back
+    used = min(R, n)
+    for pos, c in enumerate(seq):
+        prev = [p for p in range(pos) if seq[p] == c]
+        if prev:
+            gap = pos - prev[-1] - 1                         # other calls in between
+            assert gap * wb >= min(3 * l2, (used - 1) * wb), (n, pos, c, gap)
+    if n <= R:
+        assert R % n == 0                                    # whole rotations per graph
