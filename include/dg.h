@@ -100,11 +100,13 @@ typedef enum {
  *   DG_VAR_CC_BULK: [0] 0, [1] pipeline stages (0 = as many as fit), [2] CTAs per SM (0 = 1)
  *   DG_VAR_MMA:     bf16 linear and gate/up, 1..16 rows: [0] warps sharing one 16-row
  *                   group's 512-element K segments (1, 2, 4, 8; 0 = derived), [1] warps per
- *                   CTA (4 or 8; 0 = 8), [2] CTAs per SM cap (0 = occupancy limit), [3]
- *                   32-element chunks per load round (2, 4, 8; 0 = 4)
+ *                   CTA (4 or 8; 0 = derived), [2] CTAs per SM cap (0 = occupancy limit),
+ *                   [3] 32-element chunks per load round (2, 4, 8; 0 = 8 up to 8 rows,
+ *                   4 above)
  *   DG_VAR_TC:      [0] pipeline stages (0 = derived from the shape); bf16 linear and
  *                   gate/up: [1] K-split rule, 0 = sized by the shape and the row
- *                   count, 1 = by the shape alone (the batch-invariant mode's choice;
+ *                   count, 1 = by the shape alone, on a given device (the
+ *                   batch-invariant mode's choice;
  *                   the two agree up to 128 rows); A8W8: [1] 1 = quantise the activations
  *                   in a launch of its own into the workspace and stream the codes by TMA
  *                   (0 = the quantisation fused into the tensor-core kernel; same bits)
@@ -324,7 +326,8 @@ dg_status dg_moe_w2(const void* a, const int32_t* topk_ids, const float* gw, con
  * x [M, K] bf16, Wq [N, K] e4m3 codes, sw [ceil(N/128), ceil(K/128)] fp32 (one scale
  * per 128 x 128 weight block, row-major), y [M, N] bf16.  1 <= M <= 64, K % 16 == 0.
  * Runs on the tensor cores only (DG_VAR_TC; params[0] pipeline stages); the K-split
- * is fixed by (N, K), so output row m depends on input row m alone at every M.
+ * is fixed by (N, K) on a given device, so output row m depends on input row m alone
+ * at every M.
  * Non-finite activations give NaN outputs for their token.  ws: the status word, and
  * the codes and scales when the quantisation runs as a launch of its own. */
 dg_status dg_gemv_a8w8_blockscale(const void* x, const void* Wq, const float* sw, void* y, int M, int N, int K,
