@@ -9,6 +9,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <utility>
 
 #include "dg_cc_bulk.cuh"
 #include "dg_cc_dense.cuh"
@@ -22,8 +23,9 @@ namespace {
 std::mutex g_mu;
 DeviceInfo g_dev[64];
 bool g_dev_ok[64];
-std::map<std::tuple<const void*, int, size_t>, int> g_occ;
-std::map<const void*, bool> g_attr;
+// Both per device: a kernel's attributes and occupancy belong to the device it runs on.
+std::map<std::tuple<int, const void*, int, size_t>, int> g_occ;
+std::map<std::pair<int, const void*>, bool> g_attr;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -101,12 +103,17 @@ cudaError_t launch_kernel_cooperative(const void* fn, unsigned grid, unsigned bl
 
 int occupancy(const void* fn, int threads, size_t smem)
 {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_attr[fn]) {
-        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxDynSmem));
-        g_attr[fn] = true;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        dev = 0;
     }
-    auto key = std::make_tuple(fn, threads, smem);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_attr[std::make_pair(dev, fn)]) {
+        cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxDynSmem));
+        g_attr[std::make_pair(dev, fn)] = true;
+    }
+    auto key = std::make_tuple(dev, fn, threads, smem);
     auto it = g_occ.find(key);
     if (it != g_occ.end()) return it->second;
     int n = 0;

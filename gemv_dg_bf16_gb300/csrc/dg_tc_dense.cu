@@ -796,16 +796,16 @@ int cluster_capacity(const DeviceInfo* dev, bool two_per_sm, int size)
 {
     static std::mutex mu;
     static int cap[64][2][kMaxCluster + 1];
-    static bool attr_set = false;
+    static bool attr_set[64] = {};
     const int fallback = (two_per_sm ? 2 : 1) * dev->sm_count / size;
     if (size < 1 || size > kMaxCluster || dev->device < 0 || dev->device >= 64) return fallback;
     std::lock_guard<std::mutex> lk(mu);
     int& c = cap[dev->device][two_per_sm ? 1 : 0][size];
     if (c == 0) {
         const void* fn = reinterpret_cast<const void*>(&cluster_slot_kernel);
-        if (!attr_set) {
+        if (!attr_set[dev->device]) {        // the current device is dev->device
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxDynSmem));
-            attr_set = true;
+            attr_set[dev->device] = true;
         }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(static_cast<unsigned>(size * dev->sm_count));
